@@ -1,0 +1,484 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized GEMV/GEMM hot path on GB300; prints ONE JSON line.
+
+Headline workload (the metric "quant GEMV weight GB/s"): the decode GEMV,
+M = 14336, K = 4096, N = 1, fp32 x ~ N(0,1), in Q8_0 and Q4_0. One step = one
+pass of the decode hot path over one activation vector: qgemv(Q8_0) then
+qgemv(Q4_0), dequantization fused. value = weight bytes streamed per second,
+summed over all ranks (each rank runs an independent replica: the path does not
+shard across GPUs, so N > 1 is "replicas only").
+
+Timing: W warm-up steps, then exactly K steps bracketed by a barrier and a
+device synchronize, timed with CUDA events on the launching stream; each step
+is one CUDA-graph replay (the kernels are a few microseconds, shorter than a
+Python launch). L2 is defeated by rotating through weight copies totalling
+more than 3x the L2 size. Clocks are sampled with nvidia-smi during the timed
+region. The per-kernel roofline uses each kernel's average duration from a
+graph of back-to-back launches timed in the same run.
+
+--impl reference times the CPU oracle (tests' reference implementation) on
+the host cores for the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quant GEMV weight GB/s (% of HBM peak); quant GEMM TFLOP/s per kind"
+UNIT = "GB/s"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the per-kind GEMM/MoE/dequant table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK if k in d}, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = False
+
+    def init(self, backend="nccl"):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.pg = True
+
+    def barrier(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        import torch.distributed as dist
+        dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+def oracle_decode_rate(kinds, M, K, budget_s: float, threads: int):
+    """Weight GB/s of the oracle on the decode workload (full M rows per kind)."""
+    import oracle
+    from gemv_mul_mm_gb300 import synth
+    orc = oracle.load()
+    c = synth.DECODE
+    data = [(k, synth.workload_weights(c, k), synth.workload_x(c, k)) for k in kinds]
+    wbytes = sum(w.size for _, w, _ in data)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        for k, w, x in data:
+            orc.gemm(k, w, M, K, x, 1, nthreads=threads)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return wbytes * steps / el / 1e9, steps, el, wbytes
+
+
+def run_reference(a):
+    d = Dist()
+    if d.world > 1:
+        d.init("gloo")
+        if d.rank != 0:
+            d.close()
+            return
+    from gemv_mul_mm_gb300 import synth
+    import oracle
+    c = synth.DECODE
+    kinds, M, K = c["kinds"], c["M"], c["K"]
+    threads = host_cores()
+    orc = oracle.load()
+    data = [(k, synth.workload_weights(c, k), synth.workload_x(c, k)) for k in kinds]
+    rb = {k: synth.row_bytes(k, K) for k in kinds}
+
+    def step(r0, rows):
+        # one bounded sample of the decode pass: `rows` weight rows of each kind
+        for k, w, x in data:
+            orc.gemm(k, w[r0 * rb[k]:(r0 + rows) * rb[k]], rows, K, x, 1, nthreads=threads)
+
+    t0 = time.perf_counter()
+    step(0, M)
+    t_full = time.perf_counter() - t0
+    # size the sample so K steps take about a minute
+    rows = int(min(M, max(32, M * (60.0 / max(1, a.steps)) / max(t_full, 1e-6))))
+    for i in range(max(0, a.warmup)):
+        step((i * rows) % (M - rows + 1), rows)
+    t0 = time.perf_counter()
+    for i in range(a.steps):
+        step((i * rows) % (M - rows + 1), rows)
+    el = time.perf_counter() - t0
+    n_done = a.steps
+    wbytes = sum(rows * rb[k] for k in kinds)
+    value = wbytes * n_done / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": a.gpus, "steps": n_done, "warmup": a.warmup, "ms_per_step": round(el / n_done * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded splitmix64; shapes/distributions of the decode GEMV workload)",
+        "config": {"workload": "decode GEMV M=14336 K=4096 N=1, Q8_0 + Q4_0, fp32 x",
+                   "kinds": list(kinds), "weight_bytes_per_step": wbytes, "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} of {M} weight rows of each kind per step ({wbytes} weight bytes), "
+                                   f"{'OpenMP' if orc.has_openmp else 'single-thread'} over rows"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    d.close()
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gemv_mul_mm_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key: str, srcs):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("src_sha") != src_hash(*srcs):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def graph_of(fn, reps: int, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(reps):
+            fn(i)
+    return g
+
+
+def time_graph(g, replays: int, stream):
+    import torch
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(replays):
+        g.replay()
+    e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e)
+
+
+def secondary_table(qmm, synth, l2_bytes, stream, pk):
+    """Per-kind GEMM TFLOP/s, MoE and dequant GB/s (one GPU, outside the
+    headline's timed region)."""
+    import torch
+    out = {}
+
+    def bench_fn(fn, copies, reps=20, replays=5):
+        g = graph_of(lambda i: fn(i % copies), reps, stream)
+        time_graph(g, 1, stream)
+        ms = time_graph(g, replays, stream)
+        return ms / (reps * replays)
+
+    # tiny Q4_0 qgemm (latency bound)
+    c = synth.TINY
+    w = torch.from_numpy(synth.workload_weights(c, "Q4_0")).cuda()
+    x = torch.from_numpy(synth.workload_x(c, "Q4_0")).cuda()
+    y = torch.empty((c["N"], c["M"]), device="cuda")
+    ms = bench_fn(lambda i: qmm.qgemm("Q4_0", w, x, c["M"], c["K"], c["N"], Y=y, stream=stream.cuda_stream), 1)
+    out["tiny_q4_0_qgemm"] = {"us": round(ms * 1e3, 3), "path": qmm.last_path(),
+                              "tflops": round(2 * c["M"] * c["K"] * c["N"] / (ms * 1e-3) / 1e12, 4)}
+    # prefill GEMMs
+    gem = {}
+    for cfg in (synth.KQUANT, synth.CODEBOOK):
+        M, K, N = cfg["M"], cfg["K"], cfg["N"]
+        X = torch.from_numpy(synth.workload_x(cfg, cfg["kinds"][0])).cuda()
+        Y = torch.empty((N, M), device="cuda")
+        for kind in cfg["kinds"]:
+            wh = torch.from_numpy(synth.workload_weights(cfg, kind))
+            copies = max(1, math.ceil(3 * l2_bytes / wh.numel()))
+            ws = [wh.cuda() for _ in range(copies)]
+            ms = bench_fn(lambda i: qmm.qgemm(kind, ws[i], X, M, K, N, Y=Y, stream=stream.cuda_stream),
+                          copies, reps=max(copies, 6), replays=3)
+            tf = 2 * M * K * N / (ms * 1e-3) / 1e12
+            gem[kind] = {"M": M, "K": K, "N": N, "us": round(ms * 1e3, 2), "tflops": round(tf, 2),
+                         "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4), "path": qmm.last_path()}
+            del ws
+    out["gemm"] = gem
+    # MoE grouped
+    moe = {}
+    for T in synth.MOE["tokens"]:
+        p = synth.moe_problem(T, "gate_up")
+        W = torch.from_numpy(p["w"]).cuda()
+        X = torch.from_numpy(p["x"]).cuda()
+        xr = torch.from_numpy(p["x_row"]).cuda()
+        eid = torch.from_numpy(p["expert_id"]).cuda()
+        Y = torch.empty((p["x_row"].size, p["M"]), device="cuda")
+        ms = bench_fn(lambda i: qmm.qgemm_grouped(p["kind"], W, p["stride"], p["n_experts"], X, xr, eid,
+                                                  p["M"], p["K"], Y=Y, stream=stream.cuda_stream), 1)
+        distinct = len(set(p["expert_id"].tolist()))
+        gbs = distinct * p["stride"] / (ms * 1e-3) / 1e9
+        moe[f"gate_up_T{T}"] = {"us": round(ms * 1e3, 2), "distinct_experts": distinct,
+                                "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4)}
+        del W
+    out["moe_q4_0"] = moe
+    # dequant (decode-workload Q4_0 tensor)
+    c = synth.DECODE
+    wh = torch.from_numpy(synth.workload_weights(c, "Q4_0")).cuda()
+    o = torch.empty((c["M"], c["K"]), device="cuda")
+    ms = bench_fn(lambda i: qmm.qdequant("Q4_0", wh, c["M"], c["K"], out=o, stream=stream.cuda_stream), 1,
+                  reps=5, replays=3)
+    byt = wh.numel() + 4 * c["M"] * c["K"]
+    out["dequant_q4_0"] = {"us": round(ms * 1e3, 2), "gbs": round(byt / (ms * 1e-3) / 1e9, 1),
+                           "frac_of_hbm": round(byt / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+    return out
+
+
+def run_ours(a):
+    import numpy as np
+    import torch
+
+    d = Dist()
+    d.init("nccl")
+    torch.cuda.set_device(d.local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from gemv_mul_mm_gb300 import qmm, synth
+
+    pk, pk_src = peaks()
+    c = synth.DECODE
+    kinds, M, K = c["kinds"], c["M"], c["K"]
+    props = torch.cuda.get_device_properties(d.local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024))
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+
+    host_w = {k: synth.workload_weights(c, k) for k in kinds}
+    host_x = {k: synth.workload_x(c, k) for k in kinds}
+    wbytes = {k: host_w[k].size for k in kinds}
+    step_bytes = sum(wbytes.values())
+    copies = max(2, math.ceil(3 * l2 / step_bytes))
+    with torch.cuda.stream(stream):
+        W = {k: [torch.from_numpy(host_w[k]).cuda() for _ in range(copies)] for k in kinds}
+        X = {k: torch.from_numpy(host_x[k]).cuda() for k in kinds}
+        Y = {k: torch.empty(M, device="cuda") for k in kinds}
+    torch.cuda.synchronize()
+
+    def one_step(i):
+        j = i % copies
+        for k in kinds:
+            qmm.qgemv(k, W[k][j], X[k], M, K, y=Y[k], stream=sh)
+
+    # one graph per weight copy, each = one step
+    graphs = [graph_of(lambda _i, j=j: one_step(j), 1, stream) for j in range(copies)]
+    for i in range(max(3, a.warmup)):
+        graphs[i % copies].replay()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(d.local)
+    ev_s, ev_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    n0 = qmm.launch_count()
+    ev_s.record(stream)
+    for i in range(a.steps):
+        graphs[i % copies].replay()
+    ev_e.record(stream)
+    ev_e.synchronize()
+    torch.cuda.synchronize()
+    d.barrier()
+    # graph replays launch their kernels without passing through the library's
+    # launch counter: each step holds len(kinds) of our kernels.
+    launches = (qmm.launch_count() - n0) + a.steps * len(kinds)
+    clk = clocks.stop()
+    ms_total = d.max(ev_s.elapsed_time(ev_e))
+    ms_step = ms_total / a.steps
+    value = d.world * step_bytes * a.steps / (ms_total * 1e-3) / 1e9
+
+    # per-kernel durations: graphs of back-to-back launches of one kind
+    per = {}
+    R = 4 * copies
+    for k in kinds:
+        g = graph_of(lambda i, k=k: qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh), R, stream)
+        time_graph(g, 2, stream)
+        ms = time_graph(g, max(5, 2000 // R), stream) / (R * max(5, 2000 // R))
+        alg = wbytes[k] + 4 * K + 4 * M
+        per[k] = {"us": round(ms * 1e3, 3), "weight_gbs": round(wbytes[k] / (ms * 1e-3) / 1e9, 1),
+                  "achieved_gbs": round(alg / (ms * 1e-3) / 1e9, 1), "alg_bytes": alg,
+                  "frac": round(alg / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+    dom = max(kinds, key=lambda k: per[k]["us"])
+    traffic = traffic_for(f"k_gemv<{dom}>", ["k_gemv.cu", "decode.cuh", "sm100_async.cuh"])
+    roofline = {"bound": "hbm", "kernel": f"k_gemv<{dom},1>", "achieved": per[dom]["achieved_gbs"],
+                "peak": pk["hbm_gbs"], "peak_source": pk_src, "unit": "GB/s", "frac": per[dom]["frac"],
+                "traffic": traffic, "alg_bytes_per_launch": per[dom]["alg_bytes"]}
+
+    # end to end through the public API: pinned host x -> device, GEMVs, y -> pinned host
+    hx = {k: torch.from_numpy(host_x[k]).pin_memory() for k in kinds}
+    hy = {k: torch.empty(M, dtype=torch.float32).pin_memory() for k in kinds}
+    n_e2e = min(a.steps, 3000)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            for k in kinds:
+                X[k].copy_(hx[k], non_blocking=True)
+                qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh)
+                hy[k].copy_(Y[k], non_blocking=True)
+        torch.cuda.synchronize()
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_s.record(stream)
+        for i in range(n_e2e):
+            for k in kinds:
+                X[k].copy_(hx[k], non_blocking=True)
+                qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh)
+                hy[k].copy_(Y[k], non_blocking=True)
+        e_e.record(stream)
+        e_e.synchronize()
+    e2e_ms = d.max(e_s.elapsed_time(e_e))
+    e2e = {"value": round(d.world * step_bytes * n_e2e / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+           "h2d_bytes_per_step": sum(4 * K for _ in kinds), "d2h_bytes_per_step": sum(4 * M for _ in kinds),
+           "steps": n_e2e, "ms_per_step": round(e2e_ms / n_e2e, 4)}
+
+    cpu = None
+    if d.rank == 0 and d.world == 1 and not a.no_cpu_baseline:
+        cores = host_cores()
+        rate, steps, el, wb = oracle_decode_rate(kinds, M, K, 10.0, cores)
+        cpu = {"value": round(rate, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{steps} full decode steps ({wb} weight bytes each) in {el:.1f} s"}
+
+    sec = None
+    if d.rank == 0 and d.world == 1 and not a.no_secondary:
+        sec = secondary_table(qmm, synth, l2, stream, pk)
+
+    if d.rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": d.world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded splitmix64; shapes and distributions of the pages' decode workload)",
+            "config": {"workload": "decode GEMV M=14336 K=4096 N=1, Q8_0 + Q4_0, fp32 x (one step = both)",
+                       "weight_bytes_per_step": step_bytes, "parallelism": "replicas",
+                       "l2_defeat": f"rotating {copies} weight copies ({copies * step_bytes / 1e6:.0f} MB > 3x L2 "
+                                    f"{l2 / 1e6:.0f} MB)", "timing": "CUDA-graph replay per step, CUDA events"},
+            "per_kind": per, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk, "secondary": sec,
+        }
+        print(json.dumps(line), flush=True)
+    d.close()
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,257 @@
+// api.cu -- the C ABI of libqmm (include/qmm.h): argument validation, kind
+// geometry, path dispatch and the device error latch.
+//
+// Validation follows ferrox-cuda 0.21.0 src/mul_mm.rs `validate_shape`: empty
+// shapes, K not a whole number of blocks and too-small buffers are refused by
+// name before anything is launched.
+#include "../../include/qmm.h"
+#include "qmm_internal.cuh"
+
+#include <atomic>
+#include <mutex>
+
+namespace qmm {
+
+namespace {
+
+struct KindRow {
+    const char* name;
+    int block_bytes;
+    int block_elems;
+};
+
+constexpr KindRow kKinds[QMM_NKINDS] = {
+    {"Q8_0", 34, 32},   {"Q4_0", 18, 32},   {"Q5_0", 22, 32},    {"Q4_K", 144, 256},
+    {"Q5_K", 176, 256}, {"Q6_K", 210, 256}, {"Q2_K", 84, 256},   {"Q3_K", 110, 256},
+    {"IQ4_NL", 18, 32}, {"IQ4_XS", 136, 256}, {"MXFP4", 17, 32},
+};
+
+std::atomic<int> g_path{0};
+std::atomic<uint64_t> g_launches{0};
+thread_local int t_last_path = 0;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+__device__ unsigned g_dev_err;  // one latch per device (module-scope __device__)
+
+bool kind_ok(int kind) { return kind >= 0 && kind < QMM_NKINDS; }
+
+// Device latch address of the current device, looked up once per device.
+int err_ptr(unsigned** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dev_err) != cudaSuccess) return QMM_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    *out = g_err_ptr[dev];
+    return QMM_OK;
+}
+
+int finish(cudaError_t e, int path) {
+    if (e != cudaSuccess) return QMM_ERR_CUDA;
+    t_last_path = path;
+    return QMM_OK;
+}
+
+int check_x(const void* x, int x_dtype) {
+    if (x_dtype != QMM_F32 && x_dtype != QMM_F16) return QMM_ERR_BAD_DTYPE;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(x);
+    if (a % (x_dtype == QMM_F32 ? 4 : 2)) return QMM_ERR_MISALIGNED;
+    return QMM_OK;
+}
+
+}  // namespace
+
+int sm_count(int device) {
+    if (device < 0 || device >= kMaxDevices) return 1;
+    if (!g_sms[device]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) n = 1;
+        g_sms[device] = n;
+    }
+    return g_sms[device];
+}
+
+void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+int qmm_kind_info(int kind, size_t* block_bytes, size_t* block_elems) {
+    if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (!block_bytes || !block_elems) return QMM_ERR_NULL_POINTER;
+    *block_bytes = static_cast<size_t>(kKinds[kind].block_bytes);
+    *block_elems = static_cast<size_t>(kKinds[kind].block_elems);
+    return QMM_OK;
+}
+
+size_t qmm_row_bytes(int kind, int64_t K) {
+    if (!kind_ok(kind) || K <= 0 || K % kKinds[kind].block_elems) return 0;
+    return static_cast<size_t>(K / kKinds[kind].block_elems) * static_cast<size_t>(kKinds[kind].block_bytes);
+}
+
+const char* qmm_kind_name(int kind) { return kind_ok(kind) ? kKinds[kind].name : nullptr; }
+
+const char* qmm_status_str(int status) {
+    switch (status) {
+    case QMM_OK: return "ok";
+    case QMM_ERR_EMPTY_SHAPE: return "empty shape";
+    case QMM_ERR_BAD_KIND: return "unknown block format";
+    case QMM_ERR_BAD_DTYPE: return "unknown activation dtype";
+    case QMM_ERR_COLS_NOT_BLOCK_ALIGNED: return "K is not a whole number of blocks";
+    case QMM_ERR_WEIGHTS_TOO_SMALL: return "weight buffer too small";
+    case QMM_ERR_ACTIVATIONS_TOO_SMALL: return "activation buffer too small";
+    case QMM_ERR_NULL_POINTER: return "null pointer";
+    case QMM_ERR_MISALIGNED: return "misaligned pointer";
+    case QMM_ERR_BAD_EXPERT_ID: return "bad expert id, expert stride or activation row";
+    case QMM_ERR_CUDA: return "CUDA runtime error";
+    case QMM_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
+    case QMM_ERR_UNIMPLEMENTED: return "unimplemented";
+    case QMM_ERR_BAD_ARGUMENT: return "bad argument";
+    case QMM_ERR_OUTPUT_TOO_SMALL: return "output buffer too small";
+    default: return "unknown status";
+    }
+}
+
+int qmm_set_path(int path) {
+    if (path < 0 || path > 3) return -1;
+    return g_path.exchange(path);
+}
+
+int qmm_last_path(void) { return t_last_path; }
+
+uint64_t qmm_launch_count(void) { return g_launches.load(); }
+
+int qdequant(int kind, const void* blocks, size_t blocks_bytes, int64_t rows, int64_t cols,
+             float* out, size_t out_elems, void* stream) {
+    if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (rows < 0 || cols < 0) return QMM_ERR_BAD_ARGUMENT;
+    if (rows == 0 || cols == 0) return QMM_ERR_EMPTY_SHAPE;
+    if (!blocks || !out) return QMM_ERR_NULL_POINTER;
+    if (cols % kKinds[kind].block_elems) return QMM_ERR_COLS_NOT_BLOCK_ALIGNED;
+    if (reinterpret_cast<uintptr_t>(out) % 4) return QMM_ERR_MISALIGNED;
+    const size_t rb = qmm_row_bytes(kind, cols);
+    if (blocks_bytes / rb < static_cast<size_t>(rows)) return QMM_ERR_WEIGHTS_TOO_SMALL;
+    if (out_elems / static_cast<size_t>(cols) < static_cast<size_t>(rows)) return QMM_ERR_OUTPUT_TOO_SMALL;
+    const int64_t nblocks = rows * (cols / kKinds[kind].block_elems);
+    return finish(launch_dequant(kind, static_cast<const uint8_t*>(blocks), nblocks, out,
+                                 static_cast<cudaStream_t>(stream)), 4);
+}
+
+int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
+          float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream) {
+    if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (M < 0 || K < 0 || N < 0) return QMM_ERR_BAD_ARGUMENT;
+    if (M == 0 || K == 0 || N == 0) return QMM_ERR_EMPTY_SHAPE;
+    if (!W || !X || !Y) return QMM_ERR_NULL_POINTER;
+    if (int r = check_x(X, x_dtype)) return r;
+    if (reinterpret_cast<uintptr_t>(Y) % 4) return QMM_ERR_MISALIGNED;
+    if (K % kKinds[kind].block_elems) return QMM_ERR_COLS_NOT_BLOCK_ALIGNED;
+    const size_t rb = qmm_row_bytes(kind, K);
+    if (w_bytes / rb < static_cast<size_t>(M)) return QMM_ERR_WEIGHTS_TOO_SMALL;
+    if (x_elems / static_cast<size_t>(K) < static_cast<size_t>(N)) return QMM_ERR_ACTIVATIONS_TOO_SMALL;
+    if (y_elems / static_cast<size_t>(M) < static_cast<size_t>(N)) return QMM_ERR_OUTPUT_TOO_SMALL;
+    unsigned* err = nullptr;
+    if (int r = err_ptr(&err)) return r;
+
+    Problem p;
+    p.kind = kind;
+    p.W = static_cast<const uint8_t*>(W);
+    p.row_bytes = rb;
+    p.M = M;
+    p.K = K;
+    p.N = N;
+    p.X = X;
+    p.x_dtype = x_dtype;
+    p.Y = Y;
+    p.err = err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const int forced = g_path.load();
+    if (forced == 1) return finish(launch_generic(p, s), 1);
+    if (forced == 2) {
+        if (!gemv_stream_ok(p)) return QMM_ERR_UNIMPLEMENTED;
+        return finish(launch_gemv_stream(p, s), 2);
+    }
+    if (forced == 3) {
+        if (!gemm_tc_ok(p)) return QMM_ERR_UNIMPLEMENTED;
+        return finish(launch_gemm_tc(p, s), 3);
+    }
+    if (N > 8 && gemm_tc_ok(p)) return finish(launch_gemm_tc(p, s), 3);
+    if (gemv_stream_ok(p)) return finish(launch_gemv_stream(p, s), 2);
+    return finish(launch_generic(p, s), 1);
+}
+
+int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_dtype, size_t x_elems,
+          float* y, size_t y_elems, int64_t M, int64_t K, void* stream) {
+    return qgemm(kind, W, w_bytes, x, x_dtype, x_elems, y, y_elems, M, K, 1, stream);
+}
+
+int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert_stride, int n_experts,
+                  const void* X, int x_dtype, size_t x_elems, int64_t n_x_rows,
+                  const int32_t* x_row, const int32_t* expert_id, int64_t n_assign,
+                  float* Y, size_t y_elems, int64_t M, int64_t K, void* stream) {
+    if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (M < 0 || K < 0 || n_assign < 0 || n_x_rows < 0 || n_experts < 0) return QMM_ERR_BAD_ARGUMENT;
+    if (M == 0 || K == 0 || n_assign == 0) return QMM_ERR_EMPTY_SHAPE;
+    if (!W || !X || !Y || !x_row || !expert_id) return QMM_ERR_NULL_POINTER;
+    if (int r = check_x(X, x_dtype)) return r;
+    if (reinterpret_cast<uintptr_t>(Y) % 4 || reinterpret_cast<uintptr_t>(x_row) % 4 ||
+        reinterpret_cast<uintptr_t>(expert_id) % 4)
+        return QMM_ERR_MISALIGNED;
+    if (K % kKinds[kind].block_elems) return QMM_ERR_COLS_NOT_BLOCK_ALIGNED;
+    const size_t rb = qmm_row_bytes(kind, K);
+    if (n_experts == 0 || expert_stride / rb < static_cast<size_t>(M)) return QMM_ERR_BAD_EXPERT_ID;
+    // the last expert's rows must lie inside W
+    const size_t need = static_cast<size_t>(n_experts - 1) * expert_stride + static_cast<size_t>(M) * rb;
+    if (w_bytes < need) return QMM_ERR_WEIGHTS_TOO_SMALL;
+    if (n_x_rows == 0 || x_elems / static_cast<size_t>(K) < static_cast<size_t>(n_x_rows))
+        return QMM_ERR_ACTIVATIONS_TOO_SMALL;
+    if (y_elems / static_cast<size_t>(M) < static_cast<size_t>(n_assign)) return QMM_ERR_OUTPUT_TOO_SMALL;
+    unsigned* err = nullptr;
+    if (int r = err_ptr(&err)) return r;
+
+    Problem p;
+    p.kind = kind;
+    p.W = static_cast<const uint8_t*>(W);
+    p.row_bytes = rb;
+    p.M = M;
+    p.K = K;
+    p.N = n_assign;
+    p.X = X;
+    p.x_dtype = x_dtype;
+    p.Y = Y;
+    p.x_row = x_row;
+    p.expert_id = expert_id;
+    p.expert_stride = expert_stride;
+    p.n_experts = n_experts;
+    p.n_x_rows = n_x_rows;
+    p.err = err;
+    return finish(launch_generic(p, static_cast<cudaStream_t>(stream)), 1);
+}
+
+int qmm_check_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QMM_ERR_CUDA;
+    unsigned* err = nullptr;
+    if (int r = err_ptr(&err)) return r;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QMM_ERR_CUDA;
+    if (v) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return QMM_ERR_CUDA;
+    }
+    if (v & DEV_ERR_TIMEOUT) return QMM_ERR_DEVICE_TIMEOUT;
+    if (v & DEV_ERR_BAD_INDEX) return QMM_ERR_BAD_EXPERT_ID;
+    return QMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,165 @@
+// decode.cuh -- device-side block-format decoders for sm_103a.
+//
+// Each format is decoded per 32-element sub-block ("chunk" j of a block):
+// chunk j of a 256-element super-block covers elements [32j, 32j + 32), and the
+// 32-element formats have a single chunk. The byte layouts are those of the
+// pages: Vulkore examples/llm/quant_test.cpp (`ref::q8_0`, `ref::q5_0`,
+// `ref::q4_k`, `ref::q6_k`), ferrox-cuda 0.20.0 src/mul_mm_kinds/codebook.rs
+// (IQ4_NL, IQ4_XS, MXFP4 and their codebooks), ferrox-cuda 0.21.0
+// src/mul_mm.rs (Q4_0 packing, Q5_K sharing Q4_K's 6-bit scale/min unpack, the
+// Q3_K hmask bias) and, where the pages name a format without its layout
+// (Q5_K, Q2_K, Q3_K), the public GGUF block definitions.
+//
+// Arithmetic: every product is exact in fp32 (f16 scale <= 11 significant bits
+// times small integers), so any evaluation order gives the same bits; the
+// affine-min formats round once at the final subtraction. f16 -> f32 uses the
+// hardware conversion (exact, subnormals kept). Kernels are built without
+// -ftz / fast-math so fp32 subnormals (MXFP4 with small E8M0) survive.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace qmm {
+
+enum Kind : int {
+    Q8_0 = 0, Q4_0 = 1, Q5_0 = 2, Q4_K = 3, Q5_K = 4, Q6_K = 5,
+    Q2_K = 6, Q3_K = 7, IQ4_NL = 8, IQ4_XS = 9, MXFP4 = 10, NKINDS = 11
+};
+
+template <int KIND> struct Geo;
+template <> struct Geo<Q8_0>   { static constexpr int BB = 34,  BE = 32;  };
+template <> struct Geo<Q4_0>   { static constexpr int BB = 18,  BE = 32;  };
+template <> struct Geo<Q5_0>   { static constexpr int BB = 22,  BE = 32;  };
+template <> struct Geo<Q4_K>   { static constexpr int BB = 144, BE = 256; };
+template <> struct Geo<Q5_K>   { static constexpr int BB = 176, BE = 256; };
+template <> struct Geo<Q6_K>   { static constexpr int BB = 210, BE = 256; };
+template <> struct Geo<Q2_K>   { static constexpr int BB = 84,  BE = 256; };
+template <> struct Geo<Q3_K>   { static constexpr int BB = 110, BE = 256; };
+template <> struct Geo<IQ4_NL> { static constexpr int BB = 18,  BE = 32;  };
+template <> struct Geo<IQ4_XS> { static constexpr int BB = 136, BE = 256; };
+template <> struct Geo<MXFP4>  { static constexpr int BB = 17,  BE = 32;  };
+
+// 16-entry codebooks. IQ4_NL/IQ4_XS values and the E2M1 values (code 8 is
+// negative zero) as the codebook.rs page lists them.
+static __constant__ float c_kv_iq4nl[16] = {-127.f, -104.f, -83.f, -65.f, -49.f, -35.f, -22.f, -10.f,
+                                            1.f, 13.f, 25.f, 38.f, 53.f, 69.f, 89.f, 113.f};
+static __constant__ float c_kv_e2m1[16] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f,
+                                           -0.f, -0.5f, -1.f, -1.5f, -2.f, -3.f, -4.f, -6.f};
+
+__device__ __forceinline__ float h2f(uint32_t bits) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits & 0xFFFFu)));
+}
+
+// E8M0: the byte is an fp32 exponent field; 0 means 2^-127, the fp32
+// subnormal with only mantissa bit 22 set (codebook.rs, `ferrox_e8m0_to_f32`).
+__device__ __forceinline__ float e8m0f(uint32_t e) {
+    return e == 0 ? __int_as_float(0x00400000) : __int_as_float(static_cast<int>(e << 23));
+}
+
+template <typename P>
+__device__ __forceinline__ uint32_t ld8(const P* b, int o) { return reinterpret_cast<const uint8_t*>(b)[o]; }
+template <typename P>
+__device__ __forceinline__ uint32_t ld16(const P* b, int o) { return ld8(b, o) | (ld8(b, o + 1) << 8); }
+
+// Q4_K / Q5_K (scale, min) of 32-element sub-block j from the 12-byte field.
+__device__ __forceinline__ void k4_sm(const uint8_t* s, int j, int& sc, int& mn) {
+    if (j < 4) {
+        sc = s[j] & 63;
+        mn = s[j + 4] & 63;
+    } else {
+        sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
+        mn = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+// Q3_K 6-bit scale of 16-element sub-block j (unbiased value, 0..63).
+__device__ __forceinline__ int q3_scale(const uint8_t* s, int j) {
+    const int lo = (j < 8) ? (s[j] & 15) : (s[j - 8] >> 4);
+    const int hi = (s[8 + (j & 3)] >> (2 * (j >> 2))) & 3;
+    return lo | (hi << 4);
+}
+
+// Element i (0..31) of chunk j of the block at b. Byte loads only: no
+// alignment is assumed (MXFP4's 17-byte stride puts blocks on odd addresses).
+template <int KIND>
+__device__ __forceinline__ float elem32(const uint8_t* b, int j, int i) {
+    if constexpr (KIND == Q8_0) {
+        return h2f(ld16(b, 0)) * static_cast<float>(static_cast<int8_t>(b[2 + i]));
+    } else if constexpr (KIND == Q4_0 || KIND == IQ4_NL) {
+        const uint32_t byte = b[2 + (i & 15)];
+        const int c = (i < 16) ? (byte & 15) : (byte >> 4);
+        if constexpr (KIND == Q4_0) return h2f(ld16(b, 0)) * static_cast<float>(c - 8);
+        else return h2f(ld16(b, 0)) * c_kv_iq4nl[c];
+    } else if constexpr (KIND == Q5_0) {
+        const uint32_t qh = ld8(b, 2) | (ld8(b, 3) << 8) | (ld8(b, 4) << 16) | (ld8(b, 5) << 24);
+        const uint32_t byte = b[6 + (i & 15)];
+        const int lo = (i < 16) ? (byte & 15) : (byte >> 4);
+        const int q = lo | (((qh >> i) & 1) << 4);
+        return h2f(ld16(b, 0)) * static_cast<float>(q - 16);
+    } else if constexpr (KIND == Q4_K || KIND == Q5_K) {
+        int sc, mn;
+        k4_sm(b + 4, j, sc, mn);
+        const int qs = (KIND == Q4_K) ? 16 : 48;
+        const uint32_t byte = b[qs + (j >> 1) * 32 + i];
+        int q = (j & 1) ? (byte >> 4) : (byte & 15);
+        if constexpr (KIND == Q5_K) q += ((b[16 + i] >> j) & 1) << 4;
+        const float ds = h2f(ld16(b, 0)) * static_cast<float>(sc);
+        const float dm = h2f(ld16(b, 2)) * static_cast<float>(mn);
+        return __fsub_rn(__fmul_rn(ds, static_cast<float>(q)), dm);
+    } else if constexpr (KIND == Q6_K) {
+        const int h = j >> 2, g = j & 3;
+        const uint32_t lob = b[h * 64 + i + (g & 1) * 32];
+        const int lo = (g >= 2) ? (lob >> 4) : (lob & 15);
+        const int hi = (b[128 + h * 32 + i] >> (2 * g)) & 3;
+        const int sc = static_cast<int8_t>(b[192 + 2 * j + (i >> 4)]);
+        return h2f(ld16(b, 208)) * static_cast<float>(sc) * static_cast<float>((lo | (hi << 4)) - 32);
+    } else if constexpr (KIND == Q2_K) {
+        const int h = j >> 2, g = j & 3;
+        const int q = (b[16 + h * 32 + i] >> (2 * g)) & 3;
+        const int s = b[2 * j + (i >> 4)];
+        const float dl = h2f(ld16(b, 80)) * static_cast<float>(s & 15);
+        const float ml = h2f(ld16(b, 82)) * static_cast<float>(s >> 4);
+        return __fsub_rn(__fmul_rn(dl, static_cast<float>(q)), ml);
+    } else if constexpr (KIND == Q3_K) {
+        const int h = j >> 2, g = j & 3;
+        const int q2 = (b[32 + h * 32 + i] >> (2 * g)) & 3;
+        const int q = q2 - (((b[i] >> j) & 1) ? 0 : 4);
+        const int sc = q3_scale(b + 96, 2 * j + (i >> 4)) - 32;
+        return h2f(ld16(b, 108)) * static_cast<float>(sc) * static_cast<float>(q);
+    } else if constexpr (KIND == IQ4_XS) {
+        const uint32_t byte = b[8 + 16 * j + (i & 15)];
+        const int c = (i < 16) ? (byte & 15) : (byte >> 4);
+        const uint32_t sh = ld16(b, 2);
+        const int ls = ((b[4 + (j >> 1)] >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4);
+        return h2f(ld16(b, 0)) * static_cast<float>(ls - 32) * c_kv_iq4nl[c];
+    } else {  // MXFP4
+        const uint32_t byte = b[1 + (i & 15)];
+        const int c = (i < 16) ? (byte & 15) : (byte >> 4);
+        return e8m0f(b[0]) * c_kv_e2m1[c];
+    }
+}
+
+// Element e (0 <= e < BE) of the block at b.
+template <int KIND>
+__device__ __forceinline__ float elem(const uint8_t* b, int e) {
+    return elem32<KIND>(b, e >> 5, e & 31);
+}
+
+// Runtime kind -> template dispatch helper.
+#define QMM_DISPATCH_KIND(kind, FN, ...)                          \
+    switch (kind) {                                               \
+    case ::qmm::Q8_0: FN<::qmm::Q8_0>(__VA_ARGS__); break;        \
+    case ::qmm::Q4_0: FN<::qmm::Q4_0>(__VA_ARGS__); break;        \
+    case ::qmm::Q5_0: FN<::qmm::Q5_0>(__VA_ARGS__); break;        \
+    case ::qmm::Q4_K: FN<::qmm::Q4_K>(__VA_ARGS__); break;        \
+    case ::qmm::Q5_K: FN<::qmm::Q5_K>(__VA_ARGS__); break;        \
+    case ::qmm::Q6_K: FN<::qmm::Q6_K>(__VA_ARGS__); break;        \
+    case ::qmm::Q2_K: FN<::qmm::Q2_K>(__VA_ARGS__); break;        \
+    case ::qmm::Q3_K: FN<::qmm::Q3_K>(__VA_ARGS__); break;        \
+    case ::qmm::IQ4_NL: FN<::qmm::IQ4_NL>(__VA_ARGS__); break;    \
+    case ::qmm::IQ4_XS: FN<::qmm::IQ4_XS>(__VA_ARGS__); break;    \
+    default: FN<::qmm::MXFP4>(__VA_ARGS__); break;                \
+    }
+
+}  // namespace qmm

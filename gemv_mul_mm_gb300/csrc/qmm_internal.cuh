@@ -1,0 +1,57 @@
+// qmm_internal.cuh -- launchers shared between the entry points (api.cu) and
+// the kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qmm {
+
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Device-side error latch bits (OR-ed by kernels, read by qmm_check_device_error).
+enum : unsigned {
+    DEV_ERR_TIMEOUT = 1u,      // a bounded mbarrier wait ran out
+    DEV_ERR_BAD_INDEX = 2u,    // an expert id or activation row out of range
+};
+
+// Number of streaming multiprocessors of `device` (cached).
+int sm_count(int device);
+
+// Records `n` kernel launches in the process-wide counter.
+void count_launch(int n);
+
+// Problem description shared by the product kernels.
+struct Problem {
+    int kind;
+    const uint8_t* W;        // weights (expert 0 for grouped)
+    size_t row_bytes;
+    int64_t M, K, N;         // N = columns (plain) or assignments (grouped)
+    const void* X;
+    int x_dtype;             // 0 f32, 1 f16
+    float* Y;
+    // grouped only
+    const int32_t* x_row = nullptr;
+    const int32_t* expert_id = nullptr;
+    size_t expert_stride = 0;
+    int n_experts = 0;
+    int64_t n_x_rows = 0;
+    unsigned* err = nullptr; // device latch
+};
+
+// k_dequant.cu
+cudaError_t launch_dequant(int kind, const uint8_t* w, int64_t nblocks, float* out, cudaStream_t s);
+
+// k_generic.cu : CUDA-core kernels for any shape and alignment
+cudaError_t launch_generic(const Problem& p, cudaStream_t s);
+
+// k_gemv.cu : weight-streaming GEMV (bulk-copy staged rows), N <= 8 columns
+bool gemv_stream_ok(const Problem& p);
+cudaError_t launch_gemv_stream(const Problem& p, cudaStream_t s);
+
+// k_gemm_tc.cu : tcgen05 tensor-core GEMM
+bool gemm_tc_ok(const Problem& p);
+cudaError_t launch_gemm_tc(const Problem& p, cudaStream_t s);
+
+}  // namespace qmm

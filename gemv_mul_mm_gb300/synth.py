@@ -64,18 +64,37 @@ def config_seed(config: int, kind: str) -> int:
     return 20260000 + 100 * config + KIND_INDEX[kind]
 
 
-def _mix(z: np.ndarray) -> np.ndarray:
-    z = (z ^ (z >> np.uint64(30))) * _M1
-    z = (z ^ (z >> np.uint64(27))) * _M2
-    return z ^ (z >> np.uint64(31))
+def _mix_inplace(z: np.ndarray, t: np.ndarray) -> None:
+    """splitmix64 output function applied in place (t is scratch of z's size)."""
+    np.right_shift(z, np.uint64(30), out=t)
+    np.bitwise_xor(z, t, out=z)
+    np.multiply(z, _M1, out=z)
+    np.right_shift(z, np.uint64(27), out=t)
+    np.bitwise_xor(z, t, out=z)
+    np.multiply(z, _M2, out=z)
+    np.right_shift(z, np.uint64(31), out=t)
+    np.bitwise_xor(z, t, out=z)
+
+
+_CHUNK = 1 << 22
 
 
 def splitmix64(seed: int, n: int, offset: int = 0) -> np.ndarray:
-    """n outputs of splitmix64 started at `seed`, skipping the first `offset`."""
+    """n outputs of splitmix64 started at `seed`, skipping the first `offset`.
+
+    Computed in place, chunk by chunk (fresh large temporaries are slow to
+    fault in)."""
+    out = np.empty(n, dtype=np.uint64)
+    base = np.uint64(seed & 0xFFFFFFFFFFFFFFFF)
     with np.errstate(over="ignore"):
-        ctr = np.arange(offset + 1, offset + n + 1, dtype=np.uint64)
-        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + ctr * _GOLDEN
-        return _mix(z)
+        for c0 in range(0, n, _CHUNK):
+            c1 = min(n, c0 + _CHUNK)
+            z = out[c0:c1]
+            z[:] = np.arange(offset + c0 + 1, offset + c1 + 1, dtype=np.uint64)
+            np.multiply(z, _GOLDEN, out=z)
+            np.add(z, base, out=z)
+            _mix_inplace(z, np.empty_like(z))
+    return out
 
 
 def substream(seed: int, tag: int) -> int:
@@ -110,9 +129,15 @@ class Stream:
         return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
 
     def randint(self, n: int, lo: int, hi: int) -> np.ndarray:
-        """Integers uniform on [lo, hi] (inclusive)."""
-        span = np.uint64(hi - lo + 1)
-        return (self.u64(n) % span).astype(np.int64) + lo
+        """Integers uniform on [lo, hi] (inclusive).
+
+        Spans below 256 draw from 16-bit lanes of the generator (four per
+        output word; modulo bias below 0.4 %), wider spans from whole words."""
+        span = hi - lo + 1
+        if span <= 256:
+            lanes = self.u64((n + 3) // 4).view(np.uint16)[:n]
+            return (lanes % np.uint16(span)).astype(np.int16).astype(np.int64) + lo
+        return (self.u64(n) % np.uint64(span)).astype(np.int64) + lo
 
 
 def f16_bits(values: np.ndarray) -> np.ndarray:

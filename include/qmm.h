@@ -1,0 +1,205 @@
+/*
+ * qmm.h -- C ABI of libqmm: block-quantized weights times dense activations,
+ * with the dequantization fused into the kernels, on one NVIDIA GB300 (sm_103a).
+ *
+ * The problem statement follows ferrox-cuda 0.21.0 src/mul_mm.rs (the `BODY_SRC`
+ * GEMM body and `validate_shape`): a weight matrix of `M` rows, each row a run of
+ * `K / block_elems` contiguous blocks in their on-disk (GGUF) byte layout; `N`
+ * activation rows of `K` values; an fp32 output written token-major,
+ * Y[n * M + m] = sum_k W[m, k] * X[n * K + k].
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA tensors)
+ *     on the current CUDA device. The library never allocates on these paths and
+ *     never takes ownership; the caller keeps every buffer alive until the work
+ *     queued on `stream` has finished.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call
+ *     is asynchronous with respect to the host: it validates, queues kernels on
+ *     `stream` and returns.
+ *   - Errors in arguments (shape, kind, dtype, null or misaligned pointers, too
+ *     small buffers) are reported synchronously as a qmm_status BEFORE anything
+ *     is launched; nothing is written. A zero-sized shape is QMM_ERR_EMPTY_SHAPE
+ *     and launches nothing (ferrox-cuda mul_mm.rs, `MulMmUnsupported::EmptyShape`).
+ *   - A failed launch returns QMM_ERR_CUDA. Device-side conditions (a bounded
+ *     wait that ran out) are latched in a device flag and reported by
+ *     qmm_check_device_error().
+ *   - There is no fallback to a different computation and no CPU path: a format
+ *     this library does not implement is QMM_ERR_BAD_KIND (ferrox-cuda
+ *     mul_mm.rs, `kind_by_name`: the caller must fall back and say so).
+ *   - Every output element is written exactly once per call (no accumulation
+ *     into the output), so sentinel-prefilled outputs are fully overwritten.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Block formats. Geometry (bytes per block / elements per block):
+ *   Q8_0 34/32, Q4_0 18/32, Q5_0 22/32, Q4_K 144/256, Q5_K 176/256,
+ *   Q6_K 210/256, Q2_K 84/256, Q3_K 110/256, IQ4_NL 18/32, IQ4_XS 136/256,
+ *   MXFP4 17/32 (ferrox-cuda mul_mm.rs `KINDS` and its geometry test;
+ *   ferrox-cuda 0.20.0 src/mul_mm_kinds/codebook.rs for the codebook rows;
+ *   Vulkore examples/llm/quant_test.cpp `kFormats`). */
+typedef enum {
+    QMM_Q8_0 = 0,
+    QMM_Q4_0 = 1,
+    QMM_Q5_0 = 2,
+    QMM_Q4_K = 3,
+    QMM_Q5_K = 4,
+    QMM_Q6_K = 5,
+    QMM_Q2_K = 6,
+    QMM_Q3_K = 7,
+    QMM_IQ4_NL = 8,
+    QMM_IQ4_XS = 9,
+    QMM_MXFP4 = 10,
+    QMM_NKINDS = 11
+} qmm_kind;
+
+/* Activation element type. f32 activations must be 4-byte aligned, f16
+ * activations (IEEE binary16) 2-byte aligned. */
+typedef enum { QMM_F32 = 0, QMM_F16 = 1 } qmm_dtype;
+
+/* Status codes. The shape refusals mirror ferrox-cuda mul_mm.rs
+ * `MulMmUnsupported`. */
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_EMPTY_SHAPE = 1,             /* M, K, N or n_assign is 0 */
+    QMM_ERR_BAD_KIND = 2,                /* kind outside qmm_kind */
+    QMM_ERR_BAD_DTYPE = 3,               /* x_dtype outside qmm_dtype */
+    QMM_ERR_COLS_NOT_BLOCK_ALIGNED = 4,  /* K not a multiple of block_elems */
+    QMM_ERR_WEIGHTS_TOO_SMALL = 5,       /* w_bytes < M * row_bytes (or experts) */
+    QMM_ERR_ACTIVATIONS_TOO_SMALL = 6,   /* x_elems < rows needed * K */
+    QMM_ERR_NULL_POINTER = 7,
+    QMM_ERR_MISALIGNED = 8,              /* activation/output pointer alignment */
+    QMM_ERR_BAD_EXPERT_ID = 9,           /* bad n_experts / expert stride */
+    QMM_ERR_CUDA = 10,                   /* a CUDA runtime call failed */
+    QMM_ERR_DEVICE_TIMEOUT = 11,         /* a device-side bounded wait ran out */
+    QMM_ERR_UNIMPLEMENTED = 12,
+    QMM_ERR_BAD_ARGUMENT = 13,           /* negative size or other bad scalar */
+    QMM_ERR_OUTPUT_TOO_SMALL = 14        /* y_elems < outputs to write */
+} qmm_status;
+
+/* Geometry of `kind`: bytes and elements of one block. Returns QMM_OK or
+ * QMM_ERR_BAD_KIND / QMM_ERR_NULL_POINTER. Host only, no CUDA call. */
+QMM_API int qmm_kind_info(int kind, size_t* block_bytes, size_t* block_elems);
+
+/* Bytes of one weight row of K elements: (K / block_elems) * block_bytes.
+ * 0 when kind is bad or K is not a positive multiple of block_elems. */
+QMM_API size_t qmm_row_bytes(int kind, int64_t K);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+QMM_API const char* qmm_status_str(int status);
+
+/* GGUF name of a kind ("Q4_0", ...), or NULL for a bad kind. */
+QMM_API const char* qmm_kind_name(int kind);
+
+/*
+ * qdequant -- expand `rows` x `cols` quantized weights to fp32.
+ *
+ *   out[r * cols + k] = value of element k of weight row r
+ *
+ * Element values follow each format's definition (Vulkore quant_test.cpp, the
+ * `ref::` CPU references; ferrox-cuda codebook.rs for IQ4_NL / IQ4_XS / MXFP4).
+ * Bit-exact: every product in every format is exact in fp32; the affine-min
+ * formats (Q4_K, Q5_K, Q2_K) round once, at the final subtraction. No flush of
+ * subnormals (MXFP4 with small E8M0 scales yields fp32 subnormals).
+ *
+ *   blocks       device, rows * qmm_row_bytes(kind, cols) bytes, any alignment
+ *   blocks_bytes size of `blocks` in bytes (checked)
+ *   out          device fp32, rows * cols elements, 4-byte aligned
+ *   out_elems    size of `out` in elements (checked)
+ */
+QMM_API int qdequant(int kind, const void* blocks, size_t blocks_bytes, int64_t rows, int64_t cols,
+             float* out, size_t out_elems, void* stream);
+
+/*
+ * qgemv -- decode GEMV, y[m] = sum_k W[m, k] * x[k] (one activation row).
+ * Exactly qgemm with N = 1 (inferencelayer 0.2.8 src/cublas_prefill.rs,
+ * `Q4_GEMV_KERNEL`: the decode-side GEMV whose whole cost is streaming weights).
+ *
+ *   W        device, M * row_bytes bytes, any alignment (16-byte aligned W with
+ *            16-byte-multiple rows takes the streaming fast path)
+ *   w_bytes  size of W in bytes (checked)
+ *   x        device, K activations of x_dtype
+ *   x_elems  size of x in elements (checked)
+ *   y        device fp32, M elements, 4-byte aligned; y_elems its size
+ */
+QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_dtype, size_t x_elems,
+          float* y, size_t y_elems, int64_t M, int64_t K, void* stream);
+
+/*
+ * qgemm -- Y[n * M + m] = sum_k W[m, k] * X[n * K + k] for n < N, m < M
+ * (ferrox-cuda mul_mm.rs `BODY_SRC`: src0 = W, src1 = X, dst token-major).
+ * Small N runs the weight-streaming GEMV kernels; large N (and f16 activations)
+ * the tcgen05 tensor-core GEMM.
+ *
+ *   W, w_bytes   as qgemv
+ *   X            device, N * K activations of x_dtype, row-major; x_elems its size
+ *   Y            device fp32, N * M elements; y_elems its size
+ *
+ * Accuracy: |Y - Y_exact| <= 1e-3 * sum_k |W[m,k] * X[n,k]| + 1e-6 per element.
+ */
+QMM_API int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
+          float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream);
+
+/*
+ * qgemm_grouped -- expert-indexed product (a mixture-of-experts layer's
+ * routed matmul). For each assignment r < n_assign:
+ *
+ *   Y[r * M + m] = sum_k W_e[m, k] * X[x_row[r] * K + k],  e = expert_id[r]
+ *
+ * where W_e = W + e * expert_stride bytes holds expert e's M x K weights. Each
+ * assignment writes its own output row (no top-k combine).
+ *
+ *   W               device, n_experts experts of M rows each; w_bytes its size
+ *   expert_stride   bytes between experts (>= M * row_bytes)
+ *   X               device activations, n_x_rows rows of K; x_elems its size
+ *   x_row, expert_id device int32 arrays of n_assign entries. Values are read
+ *                   on the device: an out-of-range expert id or x row makes
+ *                   that assignment's output row NaN and latches
+ *                   QMM_ERR_BAD_EXPERT_ID for qmm_check_device_error().
+ *   Y               device fp32, n_assign * M elements; y_elems its size
+ */
+QMM_API int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert_stride, int n_experts,
+                  const void* X, int x_dtype, size_t x_elems, int64_t n_x_rows,
+                  const int32_t* x_row, const int32_t* expert_id, int64_t n_assign,
+                  float* Y, size_t y_elems, int64_t M, int64_t K, void* stream);
+
+/*
+ * qmm_check_device_error -- synchronize `stream`, then read and clear the
+ * device-side error latch of the current device. Returns QMM_OK,
+ * QMM_ERR_DEVICE_TIMEOUT (a bounded wait in a kernel ran out; that kernel's
+ * output is unspecified), QMM_ERR_BAD_EXPERT_ID, or QMM_ERR_CUDA.
+ */
+QMM_API int qmm_check_device_error(void* stream);
+
+/* Kernel-path override, for tests and experiments: 0 = automatic (default),
+ * 1 = force the generic CUDA-core kernels, 2 = force the streaming GEMV for
+ * qgemm (N <= 8), 3 = force the tensor-core GEMM for qgemm. Returns the
+ * previous value, or -1 for an unknown value (setting unchanged). Process-wide. */
+QMM_API int qmm_set_path(int path);
+
+/* Which kernel family the most recent successful call on this host thread
+ * launched: 1 generic, 2 streaming GEMV, 3 tensor-core GEMM, 4 dequant,
+ * 5 grouped GEMV; 0 before any call. */
+QMM_API int qmm_last_path(void);
+
+/* Number of kernels this library has launched since load (all threads). */
+QMM_API uint64_t qmm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,114 @@
+"""The C-ABI library builds, loads and exports every symbol include/qmm.h
+declares; host-side validation refuses bad arguments by name before any CUDA
+call (no GPU needed: none of these calls reaches a launch)."""
+import ctypes
+
+import pytest
+
+from gemv_mul_mm_gb300 import build as qbuild
+from gemv_mul_mm_gb300 import qmm
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return qmm.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    syms = qmm.header_symbols()
+    assert {"qdequant", "qgemv", "qgemm", "qgemm_grouped", "qmm_check_device_error"} <= set(syms)
+    for s in syms:
+        assert hasattr(L, s), f"{s} declared in qmm.h but not exported"
+
+
+def test_kind_table(L):
+    want = {"Q8_0": (34, 32), "Q4_0": (18, 32), "Q5_0": (22, 32), "Q4_K": (144, 256),
+            "Q5_K": (176, 256), "Q6_K": (210, 256), "Q2_K": (84, 256), "Q3_K": (110, 256),
+            "IQ4_NL": (18, 32), "IQ4_XS": (136, 256), "MXFP4": (17, 32)}
+    for k, g in want.items():
+        assert qmm.kind_info(k) == g
+        assert L.qmm_kind_name(qmm.KIND_ID[k]).decode() == k
+        assert qmm.row_bytes(k, 4096) == 4096 // g[1] * g[0]
+        assert qmm.row_bytes(k, g[1] + 16) == 0       # not a whole number of blocks
+    assert L.qmm_kind_name(11) is None and L.qmm_kind_name(-1) is None
+    # absent formats are not silently mapped (ferrox-cuda mul_mm.rs kind_by_name)
+    assert L.qmm_row_bytes(11, 256) == 0
+    bb, be = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.qmm_kind_info(42, ctypes.byref(bb), ctypes.byref(be)) == qmm.STATUS_ID["QMM_ERR_BAD_KIND"]
+
+
+def test_status_strings(L):
+    for code in range(15):
+        assert L.qmm_status_str(code)
+    assert L.qmm_status_str(999) == b"unknown status"
+
+
+FAKE = 0x10000  # never dereferenced: every call below is refused before a launch
+
+
+def _gemm(L, kind=1, W=FAKE, wb=1 << 30, X=FAKE, xdt=0, xe=1 << 30, Y=FAKE, ye=1 << 30,
+          M=64, K=256, N=1):
+    return L.qgemm(kind, W, wb, X, xdt, xe, Y, ye, M, K, N, None)
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(kind=11), "QMM_ERR_BAD_KIND"),
+    (dict(kind=-1), "QMM_ERR_BAD_KIND"),
+    (dict(M=0), "QMM_ERR_EMPTY_SHAPE"),
+    (dict(N=0), "QMM_ERR_EMPTY_SHAPE"),
+    (dict(K=0), "QMM_ERR_EMPTY_SHAPE"),
+    (dict(M=-3), "QMM_ERR_BAD_ARGUMENT"),
+    (dict(W=0), "QMM_ERR_NULL_POINTER"),
+    (dict(Y=0), "QMM_ERR_NULL_POINTER"),
+    (dict(xdt=7), "QMM_ERR_BAD_DTYPE"),
+    (dict(X=FAKE + 2), "QMM_ERR_MISALIGNED"),
+    (dict(Y=FAKE + 1), "QMM_ERR_MISALIGNED"),
+    (dict(K=48), "QMM_ERR_COLS_NOT_BLOCK_ALIGNED"),
+    (dict(kind=3, K=288), "QMM_ERR_COLS_NOT_BLOCK_ALIGNED"),
+    (dict(wb=64 * 144 - 1), "QMM_ERR_WEIGHTS_TOO_SMALL"),
+    (dict(xe=255), "QMM_ERR_ACTIVATIONS_TOO_SMALL"),
+    (dict(N=4, xe=3 * 256), "QMM_ERR_ACTIVATIONS_TOO_SMALL"),
+    (dict(N=2, ye=127), "QMM_ERR_OUTPUT_TOO_SMALL"),
+])
+def test_qgemm_refusals(L, args, status):
+    assert _gemm(L, **args) == qmm.STATUS_ID[status]
+
+
+def test_qgemv_and_dequant_refusals(L):
+    S = qmm.STATUS_ID
+    assert L.qgemv(1, FAKE, 1 << 30, FAKE, 0, 255, FAKE, 64, 64, 256, None) == S["QMM_ERR_ACTIVATIONS_TOO_SMALL"]
+    assert L.qgemv(1, FAKE, 1 << 30, FAKE, 1, 256, FAKE, 64, 64, 0, None) == S["QMM_ERR_EMPTY_SHAPE"]
+    assert L.qdequant(1, FAKE, 18 * 7, 2, 128, FAKE, 256, None) == S["QMM_ERR_WEIGHTS_TOO_SMALL"]
+    assert L.qdequant(1, FAKE, 18 * 8, 2, 128, FAKE, 255, None) == S["QMM_ERR_OUTPUT_TOO_SMALL"]
+    assert L.qdequant(3, FAKE, 1 << 20, 2, 100, FAKE, 1 << 20, None) == S["QMM_ERR_COLS_NOT_BLOCK_ALIGNED"]
+    assert L.qdequant(1, 0, 1 << 20, 2, 128, FAKE, 1 << 20, None) == S["QMM_ERR_NULL_POINTER"]
+    assert L.qdequant(1, FAKE, 1 << 20, 0, 128, FAKE, 1 << 20, None) == S["QMM_ERR_EMPTY_SHAPE"]
+
+
+def test_grouped_refusals(L):
+    S = qmm.STATUS_ID
+    rb = 8 * 18
+
+    def g(**kw):
+        a = dict(kind=1, W=FAKE, wb=1 << 30, stride=64 * rb, ne=4, X=FAKE, xdt=0, xe=1 << 20,
+                 nx=2, xr=FAKE, eid=FAKE, na=3, Y=FAKE, ye=1 << 20, M=64, K=256)
+        a.update(kw)
+        return L.qgemm_grouped(a["kind"], a["W"], a["wb"], a["stride"], a["ne"], a["X"], a["xdt"],
+                               a["xe"], a["nx"], a["xr"], a["eid"], a["na"], a["Y"], a["ye"],
+                               a["M"], a["K"], None)
+    assert g(na=0) == S["QMM_ERR_EMPTY_SHAPE"]
+    assert g(xr=0) == S["QMM_ERR_NULL_POINTER"]
+    assert g(eid=FAKE + 2) == S["QMM_ERR_MISALIGNED"]
+    assert g(stride=64 * rb - 1) == S["QMM_ERR_BAD_EXPERT_ID"]
+    assert g(ne=0) == S["QMM_ERR_BAD_EXPERT_ID"]
+    assert g(wb=3 * 64 * rb + 64 * rb - 1) == S["QMM_ERR_WEIGHTS_TOO_SMALL"]
+    assert g(xe=2 * 256 - 1) == S["QMM_ERR_ACTIVATIONS_TOO_SMALL"]
+    assert g(ye=3 * 64 - 1) == S["QMM_ERR_OUTPUT_TOO_SMALL"]
+
+
+def test_path_override(L):
+    assert qmm.set_path(1) == 0
+    assert qmm.set_path(0) == 1
+    assert qmm.set_path(9) == -1
+    assert qmm.set_path(0) == 0

@@ -1,0 +1,250 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Dequant: bit-exact (NaN matches NaN). GEMV/GEMM: |y - y_ref| <= 1e-3 *
+sum_k |w x| + 1e-6 per element, with every sentinel-prefilled output
+overwritten. Small shapes span several row groups / chunks and a ragged tail;
+the pages' full workloads are checked on all outputs where the oracle is fast
+and on sampled outputs otherwise.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gemv_mul_mm_gb300 import synth
+from tests.gpu_util import SENTINEL, assert_bits, assert_within, dev, sentinel
+
+pytestmark = pytest.mark.gpu
+
+KINDS = oracle.KINDS
+ELEMS = {k: synth.block_geometry(k)[1] for k in KINDS}
+
+
+@pytest.fixture(scope="module")
+def Q():
+    import torch  # noqa: F401
+    from gemv_mul_mm_gb300 import build as qbuild
+    from gemv_mul_mm_gb300 import qmm
+    qbuild.build()
+    qmm.set_path(0)
+    yield qmm
+    qmm.set_path(0)
+
+
+def raw_random_blocks(kind, rows, K, seed):
+    """Random bytes everywhere, scale fields included (NaN/Inf/subnormal scales)."""
+    n = rows * synth.row_bytes(kind, K)
+    return synth.Stream(seed).bytes(n)
+
+
+# ---------------------------------------------------------------------------
+# dequant
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("variant", ["scaled", "raw", "unaligned"])
+def test_dequant_bit_exact(Q, orc, kind, variant):
+    import torch
+    rows, cols = 131, 4 * ELEMS[kind]
+    seed = 1000 + oracle.KIND_ID[kind]
+    if variant == "raw":
+        w = raw_random_blocks(kind, rows, cols, seed)
+    else:
+        w = synth.quant_weights(kind, rows, cols, seed)
+    want = orc.dequant(kind, w, rows, cols)
+    if variant == "unaligned":
+        buf = torch.zeros(w.size + 1, dtype=torch.uint8, device="cuda")
+        buf[1:] = dev(w)
+        wd = buf[1:]
+        out = sentinel((rows, cols), offset_elems=1)
+    else:
+        wd = dev(w)
+        out = sentinel((rows, cols))
+    Q.qdequant(kind, wd, rows, cols, out=out)
+    got = out.cpu().numpy()
+    assert not np.any(got == SENTINEL)
+    assert_bits(got, want, f"{kind} {variant}")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_dequant_workload_size(Q, orc, kind):
+    """The pages' workload tensors (decode GEMV, K-quant and codebook GEMMs)."""
+    cfg = {"Q8_0": synth.DECODE, "Q4_0": synth.DECODE, "Q5_0": synth.DECODE,
+           "IQ4_NL": synth.CODEBOOK, "IQ4_XS": synth.CODEBOOK, "MXFP4": synth.CODEBOOK}.get(kind, synth.KQUANT)
+    M, K = cfg["M"], cfg["K"]
+    if kind == "Q5_0":
+        w = synth.quant_weights(kind, M, K, synth.config_seed(1, kind))
+    else:
+        w = synth.workload_weights(cfg, kind)
+    out = sentinel((M, K))
+    Q.qdequant(kind, dev(w), M, K, out=out)
+    got = out.cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(M - 8, M),
+                                     np.random.default_rng(3).integers(0, M, 256)]))
+    rb = synth.row_bytes(kind, K)
+    for r in rows:
+        want = orc.dequant(kind, w[r * rb:(r + 1) * rb], 1, K)
+        assert_bits(got[r:r + 1], want, f"{kind} row {r}")
+    assert not np.any(got == SENTINEL)
+
+
+# ---------------------------------------------------------------------------
+# GEMV / GEMM, small shapes, every path
+# ---------------------------------------------------------------------------
+def k_values(kind):
+    be = ELEMS[kind]
+    return sorted({be * 3, 2048, 4096 + 512 if be == 32 else 4096 + 2048})
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("N", [1, 3, 8, 33])
+@pytest.mark.parametrize("xdt", ["f32", "f16"])
+def test_gemm_small(Q, orc, kind, N, xdt):
+    M = 130
+    for K in k_values(kind):
+        seed = 77 + 31 * oracle.KIND_ID[kind] + K
+        w = synth.quant_weights(kind, M, K, seed)
+        x = synth.activations(N, K, seed + 1, xdt)
+        y, tol = orc.gemm(kind, w, M, K, x, N)
+        for path in (Q.PATH_AUTO, Q.PATH_GENERIC, Q.PATH_GEMV):
+            Q.set_path(path)
+            Y = sentinel((N, M))
+            try:
+                Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
+            except Q.QmmError as e:
+                assert path == Q.PATH_GEMV and e.name == "QMM_ERR_UNIMPLEMENTED"
+                continue
+            finally:
+                Q.set_path(0)
+            assert_within(Y.cpu().numpy(), y, tol, f"{kind} M={M} K={K} N={N} {xdt} path={path}")
+
+
+@pytest.mark.parametrize("kind", ["Q4_0", "Q8_0", "Q4_K", "MXFP4"])
+def test_unaligned_weights_take_generic_path(Q, orc, kind):
+    import torch
+    M, K, N = 70, 2048, 3
+    w = synth.quant_weights(kind, M, K, 5)
+    x = synth.activations(N, K, 6)
+    y, tol = orc.gemm(kind, w, M, K, x, N)
+    buf = torch.zeros(w.size + 3, dtype=torch.uint8, device="cuda")
+    buf[3:] = dev(w)
+    Y = sentinel((N, M))
+    Q.qgemm(kind, buf[3:], dev(x), M, K, N, Y=Y)
+    assert Q.last_path() == Q.PATH_GENERIC
+    assert_within(Y.cpu().numpy(), y, tol, kind)
+
+
+def test_qgemv_is_qgemm_column(Q):
+    M, K = 300, 4096
+    for kind in ("Q4_0", "Q8_0", "Q6_K"):
+        w = dev(synth.quant_weights(kind, M, K, 9))
+        x = dev(synth.activations(1, K, 10))
+        y1 = Q.qgemv(kind, w, x, M, K).cpu().numpy()
+        y2 = Q.qgemm(kind, w, x, M, K, 1).cpu().numpy()[0]
+        np.testing.assert_array_equal(y1, y2)
+
+
+# ---------------------------------------------------------------------------
+# the pages' workloads
+# ---------------------------------------------------------------------------
+def test_tiny_q4_0_qgemm(Q, orc):
+    c = synth.TINY
+    w = synth.workload_weights(c, "Q4_0")
+    x = synth.workload_x(c, "Q4_0")
+    y, tol = orc.gemm("Q4_0", w, c["M"], c["K"], x, c["N"])
+    Y = sentinel((c["N"], c["M"]))
+    Q.qgemm("Q4_0", dev(w), dev(x), c["M"], c["K"], c["N"], Y=Y)
+    assert_within(Y.cpu().numpy(), y, tol, "tiny Q4_0")
+
+
+@pytest.mark.parametrize("kind", ["Q8_0", "Q4_0"])
+def test_decode_gemv_full(Q, orc, kind):
+    c = synth.DECODE
+    M, K = c["M"], c["K"]
+    w = synth.workload_weights(c, kind)
+    x = synth.workload_x(c, kind)
+    y, tol = orc.gemm(kind, w, M, K, x, 1, nthreads=8)
+    Y = sentinel((1, M))
+    Q.qgemv(kind, dev(w), dev(x), M, K, y=Y.view(-1))
+    assert Q.last_path() == Q.PATH_GEMV
+    assert_within(Y.cpu().numpy(), y, tol, f"decode {kind}")
+
+
+def sample_positions(N, M, count, seed):
+    rng = np.random.default_rng(seed)
+    n = np.concatenate([[0, 0, N - 1, N - 1], rng.integers(0, N, count)])
+    m = np.concatenate([[0, M - 1, 0, M - 1], rng.integers(0, M, count)])
+    return n, m
+
+
+@pytest.mark.parametrize("cfg,kind", [(synth.KQUANT, k) for k in synth.KQUANT["kinds"]] +
+                         [(synth.CODEBOOK, k) for k in synth.CODEBOOK["kinds"]])
+def test_prefill_gemm_sampled(Q, orc, cfg, kind):
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    w = synth.workload_weights(cfg, kind)
+    x = synth.workload_x(cfg, kind)
+    Y = sentinel((N, M))
+    Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
+    got = Y.cpu().numpy()
+    assert not np.any(got == SENTINEL)
+    n, m = sample_positions(N, M, 400, 11)
+    y, tol = orc.gemm_at(kind, w, M, K, x, n, m)
+    assert_within(got[n, m], y, tol, f"{kind} prefill (path {Q.last_path()})")
+
+
+@pytest.mark.parametrize("T", synth.MOE["tokens"])
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+def test_moe_grouped(Q, orc, T, which):
+    p = synth.moe_problem(T, which)
+    M, K = p["M"], p["K"]
+    Y = sentinel((p["x_row"].size, M))
+    Q.qgemm_grouped(p["kind"], dev(p["w"]), p["stride"], p["n_experts"], dev(p["x"]),
+                    dev(p["x_row"]), dev(p["expert_id"]), M, K, Y=Y)
+    got = Y.cpu().numpy()
+    assert not np.any(got == SENTINEL)
+    assert Q.check_device_error() == 0
+    nr = p["x_row"].size
+    rng = np.random.default_rng(T)
+    r_idx = np.concatenate([[0, nr - 1], rng.integers(0, nr, 300)])
+    m_idx = np.concatenate([[0, M - 1], rng.integers(0, M, 300)])
+    y, tol = orc.grouped(p["kind"], p["w"], p["stride"], p["n_experts"], p["x"], p["x_row"],
+                         p["expert_id"], M, K, r_idx=r_idx, m_idx=m_idx)
+    assert_within(got[r_idx, m_idx], y, tol, f"moe {which} T={T}")
+
+
+def test_grouped_is_per_assignment_gemv(Q):
+    E, M, K = 6, 96, 512
+    rb = synth.row_bytes("Q4_0", K)
+    w = synth.quant_weights("Q4_0", E * M, K, 3)
+    x = synth.activations(5, K, 4)
+    x_row = np.array([4, 0, 0, 2, 3, 1, 4], dtype=np.int32)
+    eid = np.array([5, 0, 3, 3, 1, 2, 0], dtype=np.int32)
+    Y = Q.qgemm_grouped("Q4_0", dev(w), M * rb, E, dev(x), dev(x_row), dev(eid), M, K).cpu().numpy()
+    for r in range(x_row.size):
+        we = dev(w[eid[r] * M * rb:(eid[r] + 1) * M * rb])
+        yr = Q.qgemv("Q4_0", we, dev(x[x_row[r]]), M, K).cpu().numpy()
+        np.testing.assert_allclose(Y[r], yr, rtol=1e-5, atol=1e-5)
+
+
+def test_grouped_bad_expert_is_flagged(Q):
+    E, M, K = 2, 64, 256
+    rb = synth.row_bytes("Q4_0", K)
+    w = synth.quant_weights("Q4_0", E * M, K, 3)
+    x = synth.activations(2, K, 4)
+    x_row = np.array([0, 1, 1], dtype=np.int32)
+    eid = np.array([1, 7, 0], dtype=np.int32)      # 7 is out of range
+    Y = Q.qgemm_grouped("Q4_0", dev(w), M * rb, E, dev(x), dev(x_row), dev(eid), M, K)
+    assert Q.check_device_error() == Q.STATUS_ID["QMM_ERR_BAD_EXPERT_ID"]
+    got = Y.cpu().numpy()
+    assert np.all(np.isnan(got[1])) and np.all(np.isfinite(got[[0, 2]]))
+    assert Q.check_device_error() == 0               # the latch was cleared
+
+
+def test_empty_and_refused_shapes(Q):
+    import torch
+    w = torch.zeros(18 * 8, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(256, dtype=torch.float32, device="cuda")
+    with pytest.raises(Q.QmmError) as e:
+        Q.qgemm("Q4_0", w, x, 1, 256, 0, Y=torch.zeros(1, device="cuda"))
+    assert e.value.name == "QMM_ERR_EMPTY_SHAPE"
+    with pytest.raises(Q.QmmError) as e:
+        Q.qgemm("Q4_0", w, x, 2, 256, 1)
+    assert e.value.name == "QMM_ERR_WEIGHTS_TOO_SMALL"
