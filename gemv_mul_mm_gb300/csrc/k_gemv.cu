@@ -17,7 +17,7 @@
 //     broadcast loads. No cross-lane reduction; the NW partial sums per row
 //     are added through shared memory at the end of the row group.
 //   * Activations are staged once per CTA in a per-format layout: for Q4_0 the
-//     pairs (x[e], x[e+16] / 16) of every block, plus one offset per block, so
+//     pairs (2 x[e], x[e+16] / 8) of every block, plus one offset per block, so
 //     that a nibble OR-ed into the mantissa of 128.0f (no int->float convert)
 //     feeds a packed fp32x2 FMA (sm_100 FFMA2), and the scale d multiplies the
 //     block's partial sum in fp32.
@@ -116,10 +116,12 @@ __device__ __forceinline__ void unit_generic(const uint8_t* u, const float* xs, 
 }
 
 // Q4_0: 8 blocks of 18 bytes (144 B, 16-byte aligned in shared memory).
-// Nibble q of byte e sits at bits 16..19 (low) or 20..23 (high) after a shift;
-// OR-ing 0x43000000 gives 128 + q and 128 + 16 q exactly. Against the staged
-// pairs (x[e], x[e+16]/16) the block sum is S = sum q x + 128 X_lo + 8 X_hi,
-// so sum (q - 8) x = S - (136 X_lo + 16 X_hi) = S - cb[block].
+// Code byte e is shifted to bits 15..22 (the top of the fp32 mantissa), so
+// OR-ing 0x43000000 (128.0f) onto its low nibble gives 128 + q/2 and onto its
+// high nibble 128 + 8 q, exactly (bit 23 is the exponent's LSB and must stay
+// clear). Against the staged pairs (2 x[e], x[e+16] / 8) the block sum is
+// S = sum q x + 256 X_lo + 16 X_hi, so sum (q - 8) x = S - (264 X_lo + 24 X_hi)
+// = S - cb[block].
 template <int NCOL>
 __device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, const float* cb, int K, int k0,
                                           float (&acc)[NCOL]) {
@@ -152,9 +154,9 @@ __device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, con
                 const int bp = o + 2 + e + h;
                 const uint32_t word = w[bp >> 2];
                 const int pos = bp & 3;
-                const uint32_t t = pos == 2 ? word : pos == 0 ? (word << 16) : pos == 1 ? (word << 8) : (word >> 8);
-                const float2 f = make_float2(__int_as_float(0x43000000 | (t & 0x000F0000u)),
-                                             __int_as_float(0x43000000 | (t & 0x00F00000u)));
+                const uint32_t t = pos == 0 ? (word << 15) : pos == 1 ? (word << 7) : pos == 2 ? (word >> 1) : (word >> 9);
+                const float2 f = make_float2(__int_as_float(0x43000000 | (t & 0x00078000u)),
+                                             __int_as_float(0x43000000 | (t & 0x00780000u)));
 #pragma unroll
                 for (int n = 0; n < NCOL; ++n) {
                     const float2 xp = h ? make_float2(xv[n].z, xv[n].w) : make_float2(xv[n].x, xv[n].y);
@@ -239,12 +241,12 @@ __device__ void stage_x(const GemvArgs& a, float* xs, float* cb, int tid, int nt
                 const float xl = n < a.ncols ? load_x(a.X, a.x_dtype, static_cast<int64_t>(n) * K + 32 * b + e) : 0.f;
                 const float xh =
                     n < a.ncols ? load_x(a.X, a.x_dtype, static_cast<int64_t>(n) * K + 32 * b + 16 + e) : 0.f;
-                dst[2 * e] = xl;
-                dst[2 * e + 1] = xh * 0.0625f;
+                dst[2 * e] = 2.f * xl;
+                dst[2 * e + 1] = xh * 0.125f;
                 lo += xl;
                 hi += xh;
             }
-            cb[n * nb + b] = 136.f * lo + 16.f * hi;
+            cb[n * nb + b] = 264.f * lo + 24.f * hi;
         }
     } else {
         for (int i = tid; i < NCOL * K; i += nthr) {
