@@ -4,7 +4,7 @@
 // Validation follows ferrox-cuda 0.21.0 src/mul_mm.rs `validate_shape`: empty
 // shapes, K not a whole number of blocks and too-small buffers are refused by
 // name before anything is launched.
-#include "../../include/qmm.h"
+#include "qmm.h"
 #include "qmm_internal.cuh"
 
 #include <atomic>
@@ -27,6 +27,7 @@ constexpr KindRow kKinds[QMM_NKINDS] = {
 };
 
 std::atomic<int> g_path{0};
+std::atomic<int> g_prefetch{0};
 std::atomic<uint64_t> g_launches{0};
 thread_local int t_last_path = 0;
 
@@ -78,6 +79,8 @@ int sm_count(int device) {
     return g_sms[device];
 }
 
+bool weight_prefetch() { return g_prefetch.load(std::memory_order_relaxed) != 0; }
+
 void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
 }  // namespace qmm
@@ -128,6 +131,8 @@ int qmm_set_path(int path) {
 }
 
 int qmm_last_path(void) { return t_last_path; }
+
+int qmm_set_weight_prefetch(int on) { return g_prefetch.exchange(on ? 1 : 0); }
 
 uint64_t qmm_launch_count(void) { return g_launches.load(); }
 

@@ -19,6 +19,9 @@ enum : unsigned {
 // Number of streaming multiprocessors of `device` (cached).
 int sm_count(int device);
 
+// Whether callers declared their weights constant (qmm_set_weight_prefetch).
+bool weight_prefetch();
+
 // Records `n` kernel launches in the process-wide counter.
 void count_launch(int n);
 

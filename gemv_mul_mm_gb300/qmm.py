@@ -64,6 +64,7 @@ def _lib():
                                     _P, _SZ, _I64, _I64, _P]
         L.qmm_check_device_error.argtypes = [_P]
         L.qmm_set_path.argtypes = [_I]
+        L.qmm_set_weight_prefetch.argtypes = [_I]
         L.qmm_launch_count.restype = ctypes.c_uint64
         _LIB = L
     return _LIB
@@ -114,6 +115,11 @@ def row_bytes(kind, K: int) -> int:
 
 def set_path(path: int) -> int:
     return _lib().qmm_set_path(path)
+
+
+def set_weight_prefetch(on: bool) -> int:
+    """Declare weights constant while work is in flight (enables early weight streaming)."""
+    return _lib().qmm_set_weight_prefetch(1 if on else 0)
 
 
 def last_path() -> int:

@@ -190,6 +190,14 @@ QMM_API int qmm_check_device_error(void* stream);
  * previous value, or -1 for an unknown value (setting unchanged). Process-wide. */
 QMM_API int qmm_set_path(int path);
 
+/* Declares that weight buffers passed to later calls are not written by work
+ * still in flight on the same stream (the normal case for model weights).
+ * The streaming GEMV then starts reading W while the preceding kernel on the
+ * stream is still running (programmatic dependent launch); activations are
+ * read, and outputs written, only after that kernel has completed in either
+ * mode. Process-wide; default 0. Returns the previous value. */
+QMM_API int qmm_set_weight_prefetch(int on);
+
 /* Which kernel family the most recent successful call on this host thread
  * launched: 1 generic, 2 streaming GEMV, 3 tensor-core GEMM, 4 dequant,
  * 5 grouped GEMV; 0 before any call. */

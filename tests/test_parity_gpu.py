@@ -168,6 +168,35 @@ def test_decode_gemv_full(Q, orc, kind):
     assert_within(Y.cpu().numpy(), y, tol, f"decode {kind}")
 
 
+@pytest.mark.parametrize("kind", ["Q4_0", "Q8_0", "IQ4_NL"])
+@pytest.mark.parametrize("M", [4100, 14336])
+def test_gemv_back_to_back_with_weight_prefetch(Q, orc, kind, M):
+    """Consecutive GEMVs on one stream, weights streamed early (programmatic
+    dependent launch): each call must still see the previous call's output as
+    its input (y of call i is x of call i+1) and write every output."""
+    import torch
+    K = 4096
+    w = [synth.quant_weights(kind, M, K, 40 + i) for i in range(3)]
+    x0 = synth.activations(1, K, 41)
+    wd = [dev(wi) for wi in w]
+    prev = Q.set_weight_prefetch(True)
+    try:
+        xs = [dev(x0)]
+        for i in range(3):
+            y = sentinel((M,))
+            Q.qgemv(kind, wd[i], xs[-1], M, K, y=y)
+            xs.append((y[:K] * 0.05).contiguous())      # next input depends on this output
+        torch.cuda.synchronize()
+    finally:
+        Q.set_weight_prefetch(bool(prev))
+    for i in range(3):
+        # step i's input is what the GPU produced at step i-1
+        xin = xs[i].cpu().numpy().reshape(1, -1)
+        yref, tol = orc.gemm(kind, w[i], M, K, xin, 1)
+        got = xs[i + 1].cpu().numpy().reshape(1, -1) / 0.05
+        assert_within(got, yref[:, :K], tol[:, :K] + 1e-6 * np.abs(yref[:, :K]), f"{kind} chain step {i}")
+
+
 def sample_positions(N, M, count, seed):
     rng = np.random.default_rng(seed)
     n = np.concatenate([[0, 0, N - 1, N - 1], rng.integers(0, N, count)])
@@ -210,7 +239,7 @@ def test_moe_grouped(Q, orc, T, which):
     assert_within(got[r_idx, m_idx], y, tol, f"moe {which} T={T}")
 
 
-def test_grouped_is_per_assignment_gemv(Q):
+def test_grouped_is_per_assignment_gemv(Q, orc):
     E, M, K = 6, 96, 512
     rb = synth.row_bytes("Q4_0", K)
     w = synth.quant_weights("Q4_0", E * M, K, 3)
@@ -218,10 +247,12 @@ def test_grouped_is_per_assignment_gemv(Q):
     x_row = np.array([4, 0, 0, 2, 3, 1, 4], dtype=np.int32)
     eid = np.array([5, 0, 3, 3, 1, 2, 0], dtype=np.int32)
     Y = Q.qgemm_grouped("Q4_0", dev(w), M * rb, E, dev(x), dev(x_row), dev(eid), M, K).cpu().numpy()
+    _, tol = orc.grouped("Q4_0", w, M * rb, E, x, x_row, eid, M, K)
     for r in range(x_row.size):
         we = dev(w[eid[r] * M * rb:(eid[r] + 1) * M * rb])
         yr = Q.qgemv("Q4_0", we, dev(x[x_row[r]]), M, K).cpu().numpy()
-        np.testing.assert_allclose(Y[r], yr, rtol=1e-5, atol=1e-5)
+        # two different kernels, each within tol of the exact value
+        assert np.all(np.abs(Y[r] - yr) <= 2 * tol[r]), r
 
 
 def test_grouped_bad_expert_is_flagged(Q):
