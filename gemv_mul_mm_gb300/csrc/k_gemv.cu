@@ -294,38 +294,41 @@ __device__ __forceinline__ void unit(const uint8_t* u, const float* xs, const fl
 }
 
 template <int KIND> __host__ __device__ constexpr int cb_floats(int K, int ncol) { return KIND == Q4_0 ? ncol * (K / 32) : 0; }
+// Q4_0 stages the raw activations apart from the permuted copy.
+template <int KIND> __host__ __device__ constexpr int raw_floats(int K, int ncol) { return KIND == Q4_0 ? ncol * K : 0; }
 
 // Activation staging by the consumer threads, after the raw fp32 activations
-// are in xs (bulk copy) or straight from global memory. Q4_0 permutes each
-// block into decode order and stores 136 * (sum of the block) in cb; the
-// other formats keep the natural order.
+// are in `raw` (bulk copy; nullptr = read them from global memory). Q4_0
+// permutes each block into decode order (a permutation within 32 words, so a
+// warp's stores hit 32 distinct banks) and stores 136 * (sum of the block) in
+// cb, one block per thread with a lane-rotated walk (conflict-free); the other
+// formats keep the natural order.
 template <int KIND, int NCOL>
-__device__ void stage_x(const GemvArgs& a, float* xs, float* cb, bool in_smem, int warp, int lane, int nwarps) {
+__device__ void stage_x(const GemvArgs& a, float* xs, float* cb, const float* raw, int tid, int nthr) {
     const int K = a.K;
-    const int nb = K / 32;
+    auto xval = [&](int n, int k) -> float {
+        if (n >= a.ncols) return 0.f;
+        return raw ? raw[n * K + k] : load_x(a.X, a.x_dtype, static_cast<int64_t>(n) * K + k);
+    };
     if constexpr (KIND == Q4_0) {
-        // one warp per (column, block): lane e holds element e
-        for (int i = warp; i < NCOL * nb; i += nwarps) {
+        for (int n = 0; n < NCOL; ++n)
+            for (int k = tid; k < K; k += nthr) {
+                const int b = k >> 5, e = k & 31;
+                xs[n * K + 32 * b + q4_slot(e, (b & 1) == 0)] = xval(n, k);
+            }
+        const int nb = K / 32;
+        for (int i = tid; i < NCOL * nb; i += nthr) {
             const int n = i / nb, b = i - n * nb;
-            float v = 0.f;
-            if (n < a.ncols)
-                v = in_smem ? xs[n * K + 32 * b + lane] : load_x(a.X, a.x_dtype, static_cast<int64_t>(n) * K + 32 * b + lane);
-            float sum = v;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            __syncwarp();
-            xs[n * K + 32 * b + q4_slot(lane, (b & 1) == 0)] = v;
-            if (lane == 0) cb[n * nb + b] = 136.f * sum;
+            float sum = 0.f;
+            for (int e = 0; e < 32; ++e) sum += xval(n, 32 * b + ((e + tid) & 31));
+            cb[i] = 136.f * sum;
         }
     } else {
-        if (in_smem) {
-            for (int n = a.ncols; n < NCOL; ++n)
-                for (int k = warp * 32 + lane; k < K; k += nwarps * 32) xs[n * K + k] = 0.f;
-        } else {
-            for (int n = 0; n < NCOL; ++n)
-                for (int k = warp * 32 + lane; k < K; k += nwarps * 32)
-                    xs[n * K + k] = n < a.ncols ? load_x(a.X, a.x_dtype, static_cast<int64_t>(n) * K + k) : 0.f;
-        }
+        for (int n = 0; n < NCOL; ++n)
+            for (int k = tid; k < K; k += nthr) {
+                if (raw && n < a.ncols) continue;   // already in place
+                xs[n * K + k] = xval(n, k);
+            }
     }
 }
 
@@ -335,6 +338,7 @@ struct Smem {
     uint8_t* stage0;
     float* xs;
     float* cb;
+    float* raw;        // bulk-copy target of the activations
     float* red;        // [2][NCOL][NW][32]
     uint64_t* full;    // [kMaxStages]
     uint64_t* empty;   // [kMaxStages]
@@ -346,7 +350,8 @@ struct Smem {
     __host__ __device__ static size_t bytes(int K, int stages) {
         using G = SGeo<KIND>;
         size_t b = static_cast<size_t>(stages) * G::STAGE_B;
-        b += sizeof(float) * (static_cast<size_t>(NCOL) * K + cb_floats<KIND>(K, NCOL) + 2 * NCOL * G::NW * 32);
+        b += sizeof(float) * (static_cast<size_t>(NCOL) * K + cb_floats<KIND>(K, NCOL) + raw_floats<KIND>(K, NCOL) +
+                              2 * NCOL * G::NW * 32);
         b = (b + 7) & ~size_t(7);
         b += (2 * kMaxStages + 5) * sizeof(uint64_t) + 16;
         return b;
@@ -357,7 +362,8 @@ struct Smem {
         stage0 = base;
         xs = reinterpret_cast<float*>(base + stages * G::STAGE_B);
         cb = xs + NCOL * K;
-        red = cb + cb_floats<KIND>(K, NCOL);
+        raw = raw_floats<KIND>(K, NCOL) ? cb + cb_floats<KIND>(K, NCOL) : xs;
+        red = cb + cb_floats<KIND>(K, NCOL) + raw_floats<KIND>(K, NCOL);
         full = reinterpret_cast<uint64_t*>(
             (reinterpret_cast<uintptr_t>(red + 2 * NCOL * G::NW * 32) + 7) & ~static_cast<uintptr_t>(7));
         empty = full + kMaxStages;
@@ -421,7 +427,7 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32) k_gemv(GemvArgs a) {
                     if (bulk_x && lane == 0) {
                         const uint32_t xb = static_cast<uint32_t>(a.ncols) * K * 4u;
                         mbar_arrive_expect_tx(sm.x_full, xb);
-                        bulk_g2s(sm.xs, a.X, xb, sm.x_full);
+                        bulk_g2s(sm.raw, a.X, xb, sm.x_full);
                     }
                 }
                 if (use > 0 && !mbar_wait(&sm.empty[s], (use - 1) & 1, abort_flag, a.err)) goto drain;
@@ -436,7 +442,7 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32) k_gemv(GemvArgs a) {
                 if (waited && it == 0 && bulk_x && lane == 0) {
                     const uint32_t xb = static_cast<uint32_t>(a.ncols) * K * 4u;
                     mbar_arrive_expect_tx(sm.x_full, xb);
-                    bulk_g2s(sm.xs, a.X, xb, sm.x_full);
+                    bulk_g2s(sm.raw, a.X, xb, sm.x_full);
                 }
             }
         }
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32) k_gemv(GemvArgs a) {
             if (bulk_x && lane == 0) {
                 const uint32_t xb = static_cast<uint32_t>(a.ncols) * K * 4u;
                 mbar_arrive_expect_tx(sm.x_full, xb);
-                bulk_g2s(sm.xs, a.X, xb, sm.x_full);
+                bulk_g2s(sm.raw, a.X, xb, sm.x_full);
             }
         }
     drain:
@@ -484,7 +490,7 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32) k_gemv(GemvArgs a) {
     if (bulk_x) {
         if (!mbar_wait(sm.x_full, 0, abort_flag, a.err)) *abort_flag = 1;
     }
-    stage_x<KIND, NCOL>(a, sm.xs, sm.cb, bulk_x, warp, lane, NW);
+    stage_x<KIND, NCOL>(a, sm.xs, sm.cb, bulk_x ? sm.raw : nullptr, threadIdx.x, NW * 32);
     named_bar_sync(1, NW * 32);
 
     int it = 0, gi = 0;
@@ -565,9 +571,12 @@ cudaError_t launch_ncol(const Problem& p, cudaStream_t s) {
     const int K = static_cast<int>(p.K);
     // Prefer two CTAs per SM (more warps to hide latency); otherwise one CTA
     // with as many stages as fit.
+    // Formats with 8 consumer warps fill an SM with one deep CTA; 4-warp
+    // formats run two CTAs per SM (measured on the decode workload).
     int stages = kMaxStages, per_sm = 2;
     while (stages > 2 && Smem<KIND, NCOL>::bytes(K, stages) > kCtaSmem) --stages;
-    if (kEnvCtas == 1 || Smem<KIND, NCOL>::bytes(K, stages) > kCtaSmem) {
+    const bool one_cta = kEnvCtas == 1 || (kEnvCtas != 2 && G::NW >= 8);
+    if (one_cta || Smem<KIND, NCOL>::bytes(K, stages) > kCtaSmem) {
         per_sm = 1;
         stages = kMaxStages;
         while (stages > 2 && Smem<KIND, NCOL>::bytes(K, stages) > kSmemBudget) --stages;
