@@ -146,6 +146,111 @@ __device__ __forceinline__ float elem(const uint8_t* b, int e) {
     return elem32<KIND>(b, e >> 5, e & 31);
 }
 
+
+// ---------------------------------------------------------------------------
+// Tensor-core operand decoding: integer codes (times integer sub-scales) and
+// the fp32 scales that multiply the partial sums.
+//
+//   format  code (exact in f16 unless noted)        scale on partial sums
+//   Q8_0    q                                        d        per 32
+//   Q4_0    q - 8                                    d        per 32
+//   Q5_0    q - 16                                   d        per 32
+//   IQ4_NL  KV[c]                                    d        per 32
+//   MXFP4   E2M1[c]                                  2^(e-127) per 32
+//   Q4_K    sc_j * q            (<= 945)             d per 256;  mins: dmin * m_j
+//   Q5_K    sc_j * q            (<= 1953)            d per 256;  mins: dmin * m_j
+//   Q6_K    sc * (q - 32)       (<= 4096; rounds once above 2048)   d per 256
+//   Q2_K    (s & 15) * q        (<= 45)              d per 256;  mins: dmin * (s >> 4)
+//   Q3_K    (sc - 32) * q       (<= 128)             d per 256
+//   IQ4_XS  (ls - 32) * KV[c]   (<= 4064; rounds once above 2048)   d per 256
+// ---------------------------------------------------------------------------
+template <int KIND> struct TcGeo {
+    static constexpr bool PER32 = Geo<KIND>::BE == 32;                       // scale per 32-element block
+    static constexpr bool MINS = KIND == Q4_K || KIND == Q5_K || KIND == Q2_K;
+    static constexpr int MIN_GROUPS = KIND == Q2_K ? 16 : 8;                 // min groups per 256
+};
+
+// Code of element i (0..31) of 32-element chunk j of the block at b.
+template <int KIND>
+__device__ __forceinline__ float code32(const uint8_t* b, int j, int i) {
+    if constexpr (KIND == Q8_0) {
+        return static_cast<float>(static_cast<int8_t>(b[2 + i]));
+    } else if constexpr (KIND == Q4_0 || KIND == IQ4_NL) {
+        const uint32_t byte = b[2 + (i & 15)];
+        const int c = (i < 16) ? (byte & 15) : (byte >> 4);
+        if constexpr (KIND == Q4_0) return static_cast<float>(c - 8);
+        else return c_kv_iq4nl[c];
+    } else if constexpr (KIND == Q5_0) {
+        const uint32_t qh = ld8(b, 2) | (ld8(b, 3) << 8) | (ld8(b, 4) << 16) | (ld8(b, 5) << 24);
+        const uint32_t byte = b[6 + (i & 15)];
+        const int lo = (i < 16) ? (byte & 15) : (byte >> 4);
+        const int q = lo | static_cast<int>(((qh >> i) & 1) << 4);
+        return static_cast<float>(q - 16);
+    } else if constexpr (KIND == MXFP4) {
+        const uint32_t byte = b[1 + (i & 15)];
+        return c_kv_e2m1[(i < 16) ? (byte & 15) : (byte >> 4)];
+    } else if constexpr (KIND == Q4_K || KIND == Q5_K) {
+        int sc, mn;
+        k4_sm(b + 4, j, sc, mn);
+        const int qs = (KIND == Q4_K) ? 16 : 48;
+        const uint32_t byte = b[qs + (j >> 1) * 32 + i];
+        int q = (j & 1) ? (byte >> 4) : (byte & 15);
+        if constexpr (KIND == Q5_K) q += ((b[16 + i] >> j) & 1) << 4;
+        return static_cast<float>(sc * q);
+    } else if constexpr (KIND == Q6_K) {
+        const int h = j >> 2, g = j & 3;
+        const uint32_t lob = b[h * 64 + i + (g & 1) * 32];
+        const int lo = (g >= 2) ? (lob >> 4) : (lob & 15);
+        const int hi = (b[128 + h * 32 + i] >> (2 * g)) & 3;
+        const int sc = static_cast<int8_t>(b[192 + 2 * j + (i >> 4)]);
+        return static_cast<float>(sc * ((lo | (hi << 4)) - 32));
+    } else if constexpr (KIND == Q2_K) {
+        const int h = j >> 2, g = j & 3;
+        const int q = (b[16 + h * 32 + i] >> (2 * g)) & 3;
+        return static_cast<float>((b[2 * j + (i >> 4)] & 15) * q);
+    } else if constexpr (KIND == Q3_K) {
+        const int h = j >> 2, g = j & 3;
+        const int q2 = (b[32 + h * 32 + i] >> (2 * g)) & 3;
+        const int q = q2 - (((b[i] >> j) & 1) ? 0 : 4);
+        return static_cast<float>((q3_scale(b + 96, 2 * j + (i >> 4)) - 32) * q);
+    } else {  // IQ4_XS
+        const uint32_t byte = b[8 + 16 * j + (i & 15)];
+        const int c = (i < 16) ? (byte & 15) : (byte >> 4);
+        const uint32_t sh = ld16(b, 2);
+        const int ls = ((b[4 + (j >> 1)] >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4);
+        return static_cast<float>(ls - 32) * c_kv_iq4nl[c];
+    }
+}
+
+// fp32 scale of a 32-element block (PER32 formats).
+template <int KIND>
+__device__ __forceinline__ float scale32(const uint8_t* b) {
+    if constexpr (KIND == MXFP4) return e8m0f(b[0]);
+    else return h2f(ld16(b, 0));
+}
+
+// Super-block d and dmin (PER32 == false).
+template <int KIND>
+__device__ __forceinline__ float2 scale256(const uint8_t* b) {
+    if constexpr (KIND == Q4_K || KIND == Q5_K) return make_float2(h2f(ld16(b, 0)), h2f(ld16(b, 2)));
+    else if constexpr (KIND == Q6_K) return make_float2(h2f(ld16(b, 208)), 0.f);
+    else if constexpr (KIND == Q2_K) return make_float2(h2f(ld16(b, 80)), h2f(ld16(b, 82)));
+    else if constexpr (KIND == Q3_K) return make_float2(h2f(ld16(b, 108)), 0.f);
+    else return make_float2(h2f(ld16(b, 0)), 0.f);  // IQ4_XS
+}
+
+// Min code of group g (Q4_K/Q5_K: 8 groups of 32; Q2_K: 16 groups of 16).
+template <int KIND>
+__device__ __forceinline__ float min_code(const uint8_t* b, int g) {
+    if constexpr (KIND == Q2_K) {
+        return static_cast<float>(b[g] >> 4);
+    } else {
+        int sc, mn;
+        k4_sm(b + 4, g, sc, mn);
+        return static_cast<float>(mn);
+    }
+}
+
 // Runtime kind -> template dispatch helper.
 #define QMM_DISPATCH_KIND(kind, FN, ...)                          \
     switch (kind) {                                               \

@@ -1,10 +1,639 @@
-// k_gemm_tc.cu -- tcgen05 tensor-core quantized GEMM (prefill shapes).
+// k_gemm_tc.cu -- quantized prefill GEMM on the 5th-generation tensor cores.
+//
+// Y[n * M + m] = sum_k W[m, k] * X[n * K + k]   (ferrox-cuda 0.21.0
+// src/mul_mm.rs, `BODY_SRC`: the batched product whose K-loop that page runs
+// as an fp32 FMA over shared tiles; here the contraction runs on tcgen05).
+//
+// One CTA computes a 128 (weight rows) x 128 (tokens) tile of Y:
+//   * warp 0 (one thread) issues the TMA loads: the raw quantized bytes of the
+//     tile's 128 rows for one 256-element super-step (a 2-D tensor map over W,
+//     16-byte aligned box), the f16 activation sub-tiles (128 tokens x 64 k,
+//     128-byte swizzled, exactly the K-major layout the MMA descriptor reads),
+//     and, for the formats with mins, the per-group activation sums.
+//   * warps 2-5 (one thread per weight row) decode the raw bytes into f16
+//     INTEGER CODES -- the stored code times its integer sub-scale, or the
+//     codebook value -- written to shared memory in the same swizzled
+//     K-major layout, plus the fp32 scales of the row;
+//   * warp 1 (one elected thread) issues tcgen05.mma kind::f16 (A = codes,
+//     B = activations, both from shared memory) into fp32 TMEM accumulators,
+//     one fresh accumulator per promotion unit, double buffered;
+//   * warps 6-13 read each finished unit from TMEM (tcgen05.ld) and apply the
+//     fp32 scales to the PARTIAL SUMS: acc += d * D1 - dmin * D2 per 256-element
+//     super-block (K-quants, IQ4_XS) or acc += d * D per 32-element block
+//     (Q8_0, Q4_0, Q5_0, IQ4_NL, MXFP4), then store Y.
+// The K-quant mins (-dmin * sum_s m_s * sum_{k in s} x_k) come out of a second,
+// K = 16 (or 32) MMA per super-block: A = the integer mins, B = the per-group
+// activation sums split hi + lo in f16 (a pre-pass kernel), into accumulator D2.
+// Every wait is bounded (about a second); a timeout latches DEV_ERR_TIMEOUT and
+// the CTA unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "decode.cuh"
 #include "qmm_internal.cuh"
+#include "sm100_async.cuh"
 
 namespace qmm {
+namespace {
 
-bool gemm_tc_ok(const Problem&) { return false; }
+constexpr int BM = 128, BN = 128, KSUP = 256, KSUB = 64;
+constexpr int AS = 3, XS = 3, RS = 2;
+constexpr int kProdWarp = 0, kMmaWarp = 1, kDec0 = 2, kNumDec = 4, kEpi0 = 6, kNumEpi = 8;
+constexpr int kThreads = (kEpi0 + kNumEpi) * 32;  // 448
+constexpr int A_TILE = BM * KSUB * 2;             // 16 KB, 128B-swizzled K-major
+constexpr int X_TILE = BN * KSUB * 2;             // 16 KB
+constexpr int MIN_TILE = 128 * 32;                // 4 KB, 32B-swizzled K-major (K = 16)
+constexpr int kTmemCols = 512;
+// instruction descriptor: D f32, A/B f16, both K-major, N = 128, M = 128
+constexpr uint32_t kIdesc = (1u << 4) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
 
-cudaError_t launch_gemm_tc(const Problem&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int gcd16(int v) { return (v % 16 == 0) ? 16 : (v % 8 == 0) ? 8 : (v % 4 == 0) ? 4 : (v % 2 == 0) ? 2 : 1; }
+
+template <int KIND> struct Raw {
+    static constexpr int SBB = (KSUP / Geo<KIND>::BE) * Geo<KIND>::BB;  // bytes of one super-step of a row
+    static constexpr int MIS = (SBB % 16 == 0) ? 0 : 16 - gcd16(SBB);   // largest start offset in a 16-B line
+    static constexpr int B0 = ((SBB + MIS + 15) / 16) * 16;
+    static constexpr int BOXB = ((B0 / 16) % 2 == 1) ? B0 : B0 + 16;    // odd number of 16-B lines per row
+    static constexpr int STAGE = BM * BOXB;
+    static_assert(BOXB / 2 <= 256, "TMA box inner dimension");
+};
+
+template <int KIND> struct Mins {
+    static constexpr bool ON = TcGeo<KIND>::MINS;
+    static constexpr int G = TcGeo<KIND>::MIN_GROUPS;       // groups per super-block
+    static constexpr int KMW = 2 * G;                        // hi + lo activation sums per super-block
+    static constexpr int TILES = ON ? KMW / 16 : 0;          // K = 16 MMAs per super-block
+};
+
+struct TcArgs {
+    int M, N, K, nsup;
+    float* Y;
+    unsigned* err;
+};
+
+// ------------------------------------------------------------ device helpers
+__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// shared-memory matrix descriptors (sm_100 format, version 1), K-major
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFF) >> 4) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFF) >> 4) | (1ull << 16) | (static_cast<uint64_t>(256 >> 4) << 32) |
+           (1ull << 46) | (6ull << 61);
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Bounded wait that also honours the CTA's abort flag; false = give up.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+    if (*abort) return false;
+    return mbar_wait(bar, parity, abort, err);
+}
+
+// Waits (bounded, ignoring abort) for the phase with `parity` of a barrier.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, unsigned* err) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > (1ll << 31)) {
+            atomicOr(err, DEV_ERR_TIMEOUT);
+            return;
+        }
+    }
+}
+
+template <int KIND>
+struct Layout {
+    using R = Raw<KIND>;
+    using MN = Mins<KIND>;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_X = OFF_A + AS * A_TILE;
+    static constexpr int OFF_RAW = OFF_X + XS * X_TILE;
+    static constexpr int OFF_AMIN = (OFF_RAW + RS * R::STAGE + 1023) & ~1023;
+    static constexpr int MINB = MN::TILES * MIN_TILE;
+    static constexpr int OFF_BMIN = OFF_AMIN + 2 * MINB;
+    static constexpr int OFF_SC = OFF_BMIN + 2 * MINB;               // [2][128][8] floats
+    static constexpr int OFF_BAR = OFF_SC + 2 * BM * 8 * 4;
+    // barriers: raw_full/empty[RS], a_full/empty[AS], x_full/empty[XS], amin_full/empty[2],
+    // bmin_full/empty[2], d_full/empty[2], sc_full/empty[2], done
+    static constexpr int NBAR = 2 * RS + 2 * AS + 2 * XS + 4 + 4 + 4 + 4 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16 + 1024;               // + alignment slack
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const __grid_constant__ CUtensorMap tmB, TcArgs a) {
+    using R = Raw<KIND>;
+    using MN = Mins<KIND>;
+    using L = Layout<KIND>;
+    constexpr bool PER32 = TcGeo<KIND>::PER32;
+    constexpr int BB = Geo<KIND>::BB;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* a_tiles = smem + L::OFF_A;
+    uint8_t* x_tiles = smem + L::OFF_X;
+    uint8_t* raw = smem + L::OFF_RAW;
+    uint8_t* amin = smem + L::OFF_AMIN;
+    uint8_t* bmin = smem + L::OFF_BMIN;
+    float* sbuf = reinterpret_cast<float*>(smem + L::OFF_SC);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+    uint64_t* raw_full = bars;
+    uint64_t* raw_empty = raw_full + RS;
+    uint64_t* a_full = raw_empty + RS;
+    uint64_t* a_empty = a_full + AS;
+    uint64_t* x_full = a_empty + AS;
+    uint64_t* x_empty = x_full + XS;
+    uint64_t* amin_full = x_empty + XS;
+    uint64_t* amin_empty = amin_full + 2;
+    uint64_t* bmin_full = amin_empty + 2;
+    uint64_t* bmin_empty = bmin_full + 2;
+    uint64_t* d_full = bmin_empty + 2;
+    uint64_t* d_empty = d_full + 2;
+    uint64_t* sc_full = d_empty + 2;
+    uint64_t* sc_empty = sc_full + 2;
+    uint64_t* done = sc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+    const int nsup = a.nsup;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RS; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], kNumDec);
+        }
+        for (int i = 0; i < AS; ++i) {
+            mbar_init(&a_full[i], kNumDec);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < XS; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&amin_full[i], kNumDec);
+            mbar_init(&amin_empty[i], 1);
+            mbar_init(&bmin_full[i], 1);
+            mbar_init(&bmin_empty[i], 1);
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kNumEpi);
+            mbar_init(&sc_full[i], kNumDec);
+            mbar_init(&sc_empty[i], kNumEpi);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProdWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int sx = 0;  // X sub-steps issued
+            int s_issued = 0;
+            for (int s = 0; s < nsup; ++s) {
+                const int rs = s % RS;
+                if (s >= RS && !wait_bar(&raw_empty[rs], ((s / RS) - 1) & 1, abort_flag, a.err)) break;
+                mbar_arrive_expect_tx(&raw_full[rs], R::STAGE);
+                tma2d(raw + rs * R::STAGE, &tmW, ((s * R::SBB) & ~15) / 2, m0, &raw_full[rs]);
+                if constexpr (MN::ON) {
+                    const int b = s & 1;
+                    if (s >= 2 && !wait_bar(&bmin_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err)) break;
+                    mbar_arrive_expect_tx(&bmin_full[b], L::MINB);
+#pragma unroll
+                    for (int t = 0; t < MN::TILES; ++t)
+                        tma2d(bmin + b * L::MINB + t * MIN_TILE, &tmB, s * MN::KMW + 16 * t, n0, &bmin_full[b]);
+                }
+                s_issued = s + 1;
+                bool ok = true;
+                for (int q = 0; q < KSUP / KSUB; ++q, ++sx) {
+                    const int xs = sx % XS;
+                    if (sx >= XS && !wait_bar(&x_empty[xs], ((sx / XS) - 1) & 1, abort_flag, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&x_full[xs], X_TILE);
+                    tma2d(x_tiles + xs * X_TILE, &tmX, s * KSUP + q * KSUB, n0, &x_full[xs]);
+                }
+                if (!ok) break;
+            }
+            // every issued copy must land before the CTA retires
+            for (int s = (s_issued > RS ? s_issued - RS : 0); s < s_issued; ++s) drain_bar(&raw_full[s % RS], (s / RS) & 1, a.err);
+            for (int i = (sx > XS ? sx - XS : 0); i < sx; ++i) drain_bar(&x_full[i % XS], (i / XS) & 1, a.err);
+            if constexpr (MN::ON)
+                for (int s = (s_issued > 2 ? s_issued - 2 : 0); s < s_issued; ++s) drain_bar(&bmin_full[s & 1], (s >> 1) & 1, a.err);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int sub = 0;
+            for (int s = 0; s < nsup && !*abort_flag; ++s) {
+                for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
+                    const int as = sub % AS, xs = sub % XS;
+                    if (!wait_bar(&a_full[as], (sub / AS) & 1, abort_flag, a.err)) break;
+                    if (!wait_bar(&x_full[xs], (sub / XS) & 1, abort_flag, a.err)) break;
+                    tc_fence_after();
+                    const uint32_t abase = smem_u32(a_tiles + as * A_TILE);
+                    const uint32_t xbase = smem_u32(x_tiles + xs * X_TILE);
+#pragma unroll
+                    for (int kk = 0; kk < KSUB / 16; ++kk) {
+                        if constexpr (PER32) {
+                            const int u = 8 * s + 2 * q + (kk >> 1), b = u & 1;
+                            if ((kk & 1) == 0 && u >= 2) {
+                                if (!wait_bar(&d_empty[b], ((u >> 1) - 1) & 1, abort_flag, a.err)) break;
+                                tc_fence_after();
+                            }
+                            tc_mma(tmem + b * BN, desc_sw128(abase + 32 * kk), desc_sw128(xbase + 32 * kk), kIdesc,
+                                   kk & 1);
+                            if (kk & 1) tc_commit(&d_full[b]);
+                        } else {
+                            const int b = s & 1;
+                            if (q == 0 && kk == 0 && s >= 2) {
+                                if (!wait_bar(&d_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err)) break;
+                                tc_fence_after();
+                            }
+                            tc_mma(tmem + b * 2 * BN, desc_sw128(abase + 32 * kk), desc_sw128(xbase + 32 * kk), kIdesc,
+                                   (q | kk) != 0);
+                        }
+                    }
+                    tc_commit(&a_empty[as]);
+                    tc_commit(&x_empty[xs]);
+                }
+                if constexpr (!PER32) {
+                    const int b = s & 1;
+                    if constexpr (MN::ON) {
+                        if (!wait_bar(&amin_full[b], (s >> 1) & 1, abort_flag, a.err)) break;
+                        if (!wait_bar(&bmin_full[b], (s >> 1) & 1, abort_flag, a.err)) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int t = 0; t < MN::TILES; ++t)
+                            tc_mma(tmem + b * 2 * BN + BN, desc_sw32(smem_u32(amin + b * L::MINB + t * MIN_TILE)),
+                                   desc_sw32(smem_u32(bmin + b * L::MINB + t * MIN_TILE)), kIdesc, t);
+                        tc_commit(&amin_empty[b]);
+                        tc_commit(&bmin_empty[b]);
+                    }
+                    tc_commit(&d_full[b]);
+                }
+            }
+            // all MMAs issued by this thread are complete before TMEM is freed
+            tc_commit(done);
+            drain_bar(done, 0, a.err);
+        }
+        __syncwarp();
+    } else if (warp < kEpi0) {
+        // ------------------------------------------------------------ decoders
+        const int r = (warp - kDec0) * 32 + lane;  // weight row within the tile
+        int sub = 0;
+        for (int s = 0; s < nsup; ++s) {
+            const int rs = s % RS;
+            bool ok = wait_bar(&raw_full[rs], (s / RS) & 1, abort_flag, a.err);
+            const uint8_t* row = raw + rs * R::STAGE + r * R::BOXB + ((s * R::SBB) & 15);
+            // scales for the epilogue
+            if (ok && s >= 2) ok = wait_bar(&sc_empty[s & 1], ((s >> 1) - 1) & 1, abort_flag, a.err);
+            float* sc = sbuf + ((s & 1) * BM + r) * 8;
+            if (ok) {
+                if constexpr (PER32) {
+#pragma unroll
+                    for (int blk = 0; blk < 8; ++blk) sc[blk] = scale32<KIND>(row + blk * BB);
+                } else {
+                    const float2 dd = scale256<KIND>(row);
+                    sc[0] = dd.x;
+                    sc[1] = dd.y;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sc_full[s & 1]);
+            if constexpr (MN::ON) {
+                const int b = s & 1;
+                if (ok && s >= 2) ok = wait_bar(&amin_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err);
+                if (ok) {
+                    // A_min tile(s): 32B-swizzled K-major, 16 f16 per row per tile
+#pragma unroll
+                    for (int t = 0; t < MN::TILES; ++t) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            const int g0 = (MN::G == 8) ? (e & 7) : e, g1 = (MN::G == 8) ? ((e + 1) & 7) : e + 1;
+                            w[e / 2] = pack_h2(min_code<KIND>(row, g0), min_code<KIND>(row, g1));
+                        }
+                        uint8_t* tb = amin + b * L::MINB + t * MIN_TILE + (r >> 3) * 256 + (r & 7) * 32;
+                        const int sw = (r >> 2) & 1;
+                        *reinterpret_cast<uint4*>(tb + ((0 ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(tb + ((1 ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                    fence_proxy_async();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&amin_full[b]);
+            }
+            for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
+                const int as = sub % AS;
+                if (ok && sub >= AS) ok = wait_bar(&a_empty[as], ((sub / AS) - 1) & 1, abort_flag, a.err);
+                if (ok) {
+                    uint8_t* base = a_tiles + as * A_TILE + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll 2
+                    for (int c = 0; c < 8; ++c) {
+                        const int e0 = q * KSUB + c * 8;  // element within the super-step
+                        uint32_t w[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int e = e0 + 2 * t;
+                            float v0, v1;
+                            if constexpr (PER32) {
+                                const uint8_t* b = row + (e >> 5) * BB;
+                                v0 = code32<KIND>(b, 0, e & 31);
+                                v1 = code32<KIND>(b, 0, (e + 1) & 31);
+                            } else {
+                                v0 = code32<KIND>(row, e >> 5, e & 31);
+                                v1 = code32<KIND>(row, e >> 5, (e + 1) & 31);
+                            }
+                            w[t] = pack_h2(v0, v1);
+                        }
+                        *reinterpret_cast<uint4*>(base + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    fence_proxy_async();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[as]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[rs]);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - kEpi0;
+        const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+        const int half = ew >> 2;                  // column half: 64 columns each
+        const int r = quad * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+        for (int s = 0; s < nsup; ++s) {
+            const float* sc = sbuf + ((s & 1) * BM + r) * 8;
+            wait_bar(&sc_full[s & 1], (s >> 1) & 1, abort_flag, a.err);
+            if constexpr (PER32) {
+                for (int j = 0; j < 8; ++j) {
+                    const int u = 8 * s + j, b = u & 1;
+                    const bool ok = wait_bar(&d_full[b], (u >> 1) & 1, abort_flag, a.err);
+                    tc_fence_after();
+                    const float d = sc[j];
+                    if (ok) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            float v[16];
+                            tmem_ld16(tmem + lane_addr + b * BN + half * 64 + c * 16, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(d, v[i], acc[c * 16 + i]);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&d_empty[b]);
+                }
+            } else {
+                const int b = s & 1;
+                const bool ok = wait_bar(&d_full[b], (s >> 1) & 1, abort_flag, a.err);
+                tc_fence_after();
+                const float d = sc[0], dm = sc[1];
+                if (ok) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float v[16];
+                        tmem_ld16(tmem + lane_addr + b * 2 * BN + half * 64 + c * 16, v);
+                        if constexpr (MN::ON) {
+                            float w2[16];
+                            tmem_ld16(tmem + lane_addr + b * 2 * BN + BN + half * 64 + c * 16, w2);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                acc[c * 16 + i] = fmaf(-dm, w2[i], fmaf(d, v[i], acc[c * 16 + i]));
+                        } else {
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(d, v[i], acc[c * 16 + i]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&d_empty[b]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sc_empty[s & 1]);
+        }
+        const int m = m0 + r;
+        if (m < a.M && !*abort_flag) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int n = n0 + half * 64 + i;
+                if (n < a.N) a.Y[static_cast<int64_t>(n) * a.M + m] = acc[i];
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// Per-group activation sums for the min term: out[n][s][0..G) = hi, [G..2G) = lo
+// with hi = f16(sum), lo = f16(sum - hi); groups of 32 (Q4_K, Q5_K) or 16 (Q2_K).
+__global__ void k_xsums(const __half* __restrict__ X, int N, int K, int gsize, int G, __half* __restrict__ out) {
+    const int ngroups = K / gsize;
+    const int64_t total = static_cast<int64_t>(N) * ngroups;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int n = static_cast<int>(i / ngroups), g = static_cast<int>(i % ngroups);
+        const __half* x = X + static_cast<int64_t>(n) * K + static_cast<int64_t>(g) * gsize;
+        float sum = 0.f;
+        for (int e = 0; e < gsize; ++e) sum += __half2float(x[e]);
+        const __half hi = __float2half_rn(sum);
+        const __half lo = __float2half_rn(sum - __half2float(hi));
+        const int s = g / G, gi = g % G;
+        __half* o = out + (static_cast<int64_t>(n) * (K / KSUP) + s) * (2 * G);
+        o[gi] = hi;
+        o[G + gi] = lo;
+    }
+}
+
+// ------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+              uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride1_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Library-owned per-device workspace for the activation sums (grown on demand;
+// the first call at a given size must not be inside stream capture).
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+Workspace g_ws[64];
+std::mutex g_ws_mu;
+
+void* workspace(size_t bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace& w = g_ws[dev];
+    if (w.bytes < bytes) {
+        if (w.ptr) cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (cudaMalloc(&w.ptr, bytes) != cudaSuccess) return nullptr;
+        w.bytes = bytes;
+    }
+    return w.ptr;
+}
+
+template <int KIND>
+void ok_kind(const Problem& p, bool* out) {
+    *out = !p.x_row && p.x_dtype == 1 && p.K % KSUP == 0 && p.row_bytes % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(p.W) % 16 == 0 && reinterpret_cast<uintptr_t>(p.X) % 16 == 0 &&
+           p.M <= (int64_t(1) << 30) && p.N <= (int64_t(1) << 30) && p.K <= (int64_t(1) << 30) && encode_fn();
+}
+
+template <int KIND>
+void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
+    using R = Raw<KIND>;
+    using MN = Mins<KIND>;
+    using L = Layout<KIND>;
+    const int M = static_cast<int>(p.M), N = static_cast<int>(p.N), K = static_cast<int>(p.K);
+    const int nsup = K / KSUP;
+    CUtensorMap tmW, tmX, tmB;
+    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, p.row_bytes / 2, M, p.row_bytes, R::BOXB / 2, BM,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.X, K, N, static_cast<uint64_t>(K) * 2, KSUB, BN,
+                  CU_TENSOR_MAP_SWIZZLE_128B)) {
+        *e = cudaErrorInvalidValue;
+        return;
+    }
+    tmB = tmX;
+    if constexpr (MN::ON) {
+        const size_t ws_bytes = static_cast<size_t>(N) * nsup * MN::KMW * 2;
+        void* ws = workspace(ws_bytes);
+        if (!ws) {
+            *e = cudaErrorMemoryAllocation;
+            return;
+        }
+        const int threads = 256;
+        const int64_t total = static_cast<int64_t>(N) * (K / (KSUP / MN::G));
+        const int blocks = static_cast<int>(imin64((total + threads - 1) / threads, 4096));
+        k_xsums<<<blocks, threads, 0, s>>>(static_cast<const __half*>(p.X), N, K, KSUP / MN::G, MN::G,
+                                           static_cast<__half*>(ws));
+        count_launch(1);
+        if ((*e = cudaGetLastError()) != cudaSuccess) return;
+        if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws, static_cast<uint64_t>(nsup) * MN::KMW, N,
+                      static_cast<uint64_t>(nsup) * MN::KMW * 2, 16, BN, CU_TENSOR_MAP_SWIZZLE_32B)) {
+            *e = cudaErrorInvalidValue;
+            return;
+        }
+    }
+    auto kern = k_gemm_tc<KIND>;
+    if ((*e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES)) != cudaSuccess) return;
+    TcArgs a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.nsup = nsup;
+    a.Y = p.Y;
+    a.err = p.err;
+    const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);
+    kern<<<grid, kThreads, L::BYTES, s>>>(tmW, tmX, tmB, a);
+    count_launch(1);
+    *e = cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_tc_ok(const Problem& p) {
+    bool ok = false;
+    QMM_DISPATCH_KIND(p.kind, ok_kind, p, &ok);
+    return ok;
+}
+
+cudaError_t launch_gemm_tc(const Problem& p, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    QMM_DISPATCH_KIND(p.kind, run, p, s, &e);
+    return e;
+}
 
 }  // namespace qmm
