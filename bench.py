@@ -283,6 +283,9 @@ def secondary_table(qmm, synth, l2_bytes, stream, pk):
     out = {}
 
     def bench_fn(fn, copies, reps=20, replays=5):
+        with torch.cuda.stream(stream):
+            fn(0)                      # first call outside capture (workspace growth)
+        torch.cuda.synchronize()
         g = graph_of(lambda i: fn(i % copies), reps, stream)
         time_graph(g, 1, stream)
         ms = time_graph(g, replays, stream)

@@ -55,6 +55,7 @@ int err_ptr(unsigned** out) {
 }
 
 int finish(cudaError_t e, int path) {
+    if (e == cudaErrorStreamCaptureUnsupported) return QMM_ERR_WORKSPACE_IN_CAPTURE;
     if (e != cudaSuccess) return QMM_ERR_CUDA;
     t_last_path = path;
     return QMM_OK;
@@ -121,6 +122,9 @@ const char* qmm_status_str(int status) {
     case QMM_ERR_UNIMPLEMENTED: return "unimplemented";
     case QMM_ERR_BAD_ARGUMENT: return "bad argument";
     case QMM_ERR_OUTPUT_TOO_SMALL: return "output buffer too small";
+    case QMM_ERR_WORKSPACE_IN_CAPTURE:
+        return "the library's workspace must grow, which cannot happen during stream capture: "
+               "make one call of this shape outside capture first";
     default: return "unknown status";
     }
 }

@@ -549,12 +549,19 @@ struct Workspace {
 Workspace g_ws[64];
 std::mutex g_ws_mu;
 
-void* workspace(size_t bytes) {
+void* workspace(size_t bytes, cudaStream_t s, bool* capturing) {
     int dev = 0;
+    *capturing = false;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Workspace& w = g_ws[dev];
     if (w.bytes < bytes) {
+        // growing would allocate: not allowed while the stream is being captured
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            *capturing = true;
+            return nullptr;
+        }
         if (w.ptr) cudaFree(w.ptr);
         w.ptr = nullptr;
         w.bytes = 0;
@@ -589,9 +596,10 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     tmB = tmX;
     if constexpr (MN::ON) {
         const size_t ws_bytes = static_cast<size_t>(N) * nsup * MN::KMW * 2;
-        void* ws = workspace(ws_bytes);
+        bool capturing = false;
+        void* ws = workspace(ws_bytes, s, &capturing);
         if (!ws) {
-            *e = cudaErrorMemoryAllocation;
+            *e = capturing ? cudaErrorStreamCaptureUnsupported : cudaErrorMemoryAllocation;
             return;
         }
         const int threads = 256;

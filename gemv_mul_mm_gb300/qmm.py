@@ -27,6 +27,7 @@ STATUS = {
     6: "QMM_ERR_ACTIVATIONS_TOO_SMALL", 7: "QMM_ERR_NULL_POINTER", 8: "QMM_ERR_MISALIGNED",
     9: "QMM_ERR_BAD_EXPERT_ID", 10: "QMM_ERR_CUDA", 11: "QMM_ERR_DEVICE_TIMEOUT",
     12: "QMM_ERR_UNIMPLEMENTED", 13: "QMM_ERR_BAD_ARGUMENT", 14: "QMM_ERR_OUTPUT_TOO_SMALL",
+    15: "QMM_ERR_WORKSPACE_IN_CAPTURE",
 }
 STATUS_ID = {v: k for k, v in STATUS.items()}
 

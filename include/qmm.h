@@ -87,7 +87,8 @@ typedef enum {
     QMM_ERR_DEVICE_TIMEOUT = 11,         /* a device-side bounded wait ran out */
     QMM_ERR_UNIMPLEMENTED = 12,
     QMM_ERR_BAD_ARGUMENT = 13,           /* negative size or other bad scalar */
-    QMM_ERR_OUTPUT_TOO_SMALL = 14        /* y_elems < outputs to write */
+    QMM_ERR_OUTPUT_TOO_SMALL = 14,       /* y_elems < outputs to write */
+    QMM_ERR_WORKSPACE_IN_CAPTURE = 15    /* workspace would grow during stream capture */
 } qmm_status;
 
 /* Geometry of `kind`: bytes and elements of one block. Returns QMM_OK or
@@ -149,6 +150,13 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
  *   Y            device fp32, N * M elements; y_elems its size
  *
  * Accuracy: |Y - Y_exact| <= 1e-3 * sum_k |W[m,k] * X[n,k]| + 1e-6 per element.
+ *
+ * Workspace: the tensor-core path for Q4_K, Q5_K and Q2_K stores per-group
+ * activation sums (N * K/16 f16 values at most) in a per-device workspace the
+ * library owns and grows on demand (cudaMalloc). Growth is refused during
+ * stream capture (QMM_ERR_WORKSPACE_IN_CAPTURE): make one call of the largest
+ * shape before capturing. Concurrent calls on different streams of one device
+ * share that workspace and must not overlap.
  */
 QMM_API int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
           float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream);
