@@ -122,6 +122,8 @@ const char* qmm_status_str(int status) {
     case QMM_ERR_UNIMPLEMENTED: return "unimplemented";
     case QMM_ERR_BAD_ARGUMENT: return "bad argument";
     case QMM_ERR_OUTPUT_TOO_SMALL: return "output buffer too small";
+    case QMM_ERR_NOALLOC_LIMIT:
+        return "problem needs more scratch than qgemm_noalloc's fixed array holds";
     case QMM_ERR_WORKSPACE_IN_CAPTURE:
         return "the library's workspace must grow, which cannot happen during stream capture: "
                "make one call of this shape outside capture first";
@@ -246,6 +248,38 @@ int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert_stride,
     p.n_x_rows = n_x_rows;
     p.err = err;
     return finish(launch_generic(p, static_cast<cudaStream_t>(stream)), 1);
+}
+
+int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
+                  float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream) {
+    if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (M < 0 || K < 0 || N < 0) return QMM_ERR_BAD_ARGUMENT;
+    if (M == 0 || K == 0 || N == 0) return QMM_ERR_EMPTY_SHAPE;
+    if (!W || !X || !Y) return QMM_ERR_NULL_POINTER;
+    if (int r = check_x(X, x_dtype)) return r;
+    if (reinterpret_cast<uintptr_t>(Y) % 4) return QMM_ERR_MISALIGNED;
+    if (K % kKinds[kind].block_elems) return QMM_ERR_COLS_NOT_BLOCK_ALIGNED;
+    const size_t rb = qmm_row_bytes(kind, K);
+    if (w_bytes / rb < static_cast<size_t>(M)) return QMM_ERR_WEIGHTS_TOO_SMALL;
+    if (x_elems / static_cast<size_t>(K) < static_cast<size_t>(N)) return QMM_ERR_ACTIVATIONS_TOO_SMALL;
+    if (y_elems / static_cast<size_t>(M) < static_cast<size_t>(N)) return QMM_ERR_OUTPUT_TOO_SMALL;
+    unsigned* err = nullptr;
+    if (int r = err_ptr(&err)) return r;
+    Problem p;
+    p.kind = kind;
+    p.W = static_cast<const uint8_t*>(W);
+    p.row_bytes = rb;
+    p.M = M;
+    p.K = K;
+    p.N = N;
+    p.X = X;
+    p.x_dtype = x_dtype;
+    p.Y = Y;
+    p.err = err;
+    if (!gemm_tc_ok(p)) return QMM_ERR_UNIMPLEMENTED;
+    const int r = launch_gemm_tc_noalloc(p, static_cast<cudaStream_t>(stream));
+    if (r == QMM_OK) t_last_path = 3;
+    return r;
 }
 
 int qmm_check_device_error(void* stream) {

@@ -630,7 +630,105 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     *e = cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant (qgemm_noalloc). Its scratch -- the per-group
+// activation sums of the formats with mins -- lives in this fixed device
+// array instead of the library's cudaMalloc-grown workspace. The array is
+// reserved on every GPU that loads the library until the process exits, and
+// every call shares it, so calls that overlap on the GPU race on it.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (host code cannot use the array's name as a device address).
+cudaError_t noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+template <int KIND>
+void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
+    using R = Raw<KIND>;
+    using MN = Mins<KIND>;
+    using L = Layout<KIND>;
+    const int M = static_cast<int>(p.M), N = static_cast<int>(p.N), K = static_cast<int>(p.K);
+    const int nsup = K / KSUP;
+    *status = 0;
+    CUtensorMap tmW, tmX, tmB;
+    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, p.row_bytes / 2, M, p.row_bytes, R::BOXB / 2, BM,
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.X, K, N, static_cast<uint64_t>(K) * 2, KSUB, BN,
+                  CU_TENSOR_MAP_SWIZZLE_128B)) {
+        *status = 10;  // QMM_ERR_CUDA
+        return;
+    }
+    tmB = tmX;
+    if constexpr (MN::ON) {
+        const size_t need = static_cast<size_t>(N) * nsup * MN::KMW * 2;
+        if (need > kNoAllocScratchBytes) {
+            *status = 16;  // QMM_ERR_NOALLOC_LIMIT
+            return;
+        }
+        void* ws = nullptr;
+        if (noalloc_scratch(&ws) != cudaSuccess) {
+            *status = 10;
+            return;
+        }
+        // k_xsums writes every entry of the region this call reads, so nothing
+        // left by an earlier call is ever used.
+        const int threads = 256;
+        const int64_t total = static_cast<int64_t>(N) * (K / (KSUP / MN::G));
+        const int blocks = static_cast<int>(imin64((total + threads - 1) / threads, 4096));
+        k_xsums<<<blocks, threads, 0, s>>>(static_cast<const __half*>(p.X), N, K, KSUP / MN::G, MN::G,
+                                           static_cast<__half*>(ws));
+        count_launch(1);
+        if (cudaGetLastError() != cudaSuccess ||
+            !make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws, static_cast<uint64_t>(nsup) * MN::KMW, N,
+                      static_cast<uint64_t>(nsup) * MN::KMW * 2, 16, BN, CU_TENSOR_MAP_SWIZZLE_32B)) {
+            *status = 10;
+            return;
+        }
+    }
+    auto kern = k_gemm_tc<KIND>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) != cudaSuccess) {
+        *status = 10;
+        return;
+    }
+    TcArgs a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.nsup = nsup;
+    a.Y = p.Y;
+    a.err = p.err;
+    const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);
+    kern<<<grid, kThreads, L::BYTES, s>>>(tmW, tmX, tmB, a);
+    count_launch(1);
+    if (cudaGetLastError() != cudaSuccess) *status = 10;
+}
+
 }  // namespace
+
+int launch_gemm_tc_noalloc(const Problem& p, cudaStream_t s) {
+    int status = 0;
+    QMM_DISPATCH_KIND(p.kind, run_noalloc, p, s, &status);
+    return status;
+}
 
 bool gemm_tc_ok(const Problem& p) {
     bool ok = false;

@@ -56,5 +56,8 @@ cudaError_t launch_gemv_stream(const Problem& p, cudaStream_t s);
 // k_gemm_tc.cu : tcgen05 tensor-core GEMM
 bool gemm_tc_ok(const Problem& p);
 cudaError_t launch_gemm_tc(const Problem& p, cudaStream_t s);
+// Same GEMM with its scratch in a fixed device array (no allocation);
+// returns a qmm_status code.
+int launch_gemm_tc_noalloc(const Problem& p, cudaStream_t s);
 
 }  // namespace qmm

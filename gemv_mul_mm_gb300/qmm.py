@@ -27,7 +27,7 @@ STATUS = {
     6: "QMM_ERR_ACTIVATIONS_TOO_SMALL", 7: "QMM_ERR_NULL_POINTER", 8: "QMM_ERR_MISALIGNED",
     9: "QMM_ERR_BAD_EXPERT_ID", 10: "QMM_ERR_CUDA", 11: "QMM_ERR_DEVICE_TIMEOUT",
     12: "QMM_ERR_UNIMPLEMENTED", 13: "QMM_ERR_BAD_ARGUMENT", 14: "QMM_ERR_OUTPUT_TOO_SMALL",
-    15: "QMM_ERR_WORKSPACE_IN_CAPTURE",
+    15: "QMM_ERR_WORKSPACE_IN_CAPTURE", 16: "QMM_ERR_NOALLOC_LIMIT",
 }
 STATUS_ID = {v: k for k, v in STATUS.items()}
 
@@ -61,6 +61,7 @@ def _lib():
         L.qdequant.argtypes = [_I, _P, _SZ, _I64, _I64, _P, _SZ, _P]
         L.qgemv.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _P]
         L.qgemm.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _I64, _P]
+        L.qgemm_noalloc.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _I64, _P]
         L.qgemm_grouped.argtypes = [_I, _P, _SZ, _SZ, _I, _P, _I, _SZ, _I64, _P, _P, _I64,
                                     _P, _SZ, _I64, _I64, _P]
         L.qmm_check_device_error.argtypes = [_P]
@@ -156,6 +157,18 @@ def qgemm(kind, W, X, M: int, K: int, N: int, Y=None, stream=None):
         Y = torch.empty((N, M), dtype=torch.float32, device=W.device)
     _check(_lib().qgemm(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(X), _xdt(X),
                         X.numel(), _ptr(Y), Y.numel(), M, K, N, _stream(stream)), "qgemm")
+    return Y
+
+
+def qgemm_noalloc(kind, W, X, M: int, K: int, N: int, Y=None, stream=None):
+    """qgemm on the tensor-core path without any device allocation by the
+    library (scratch in a fixed device array); Y must be given by callers that
+    cannot allocate either."""
+    import torch
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=W.device)
+    _check(_lib().qgemm_noalloc(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(X), _xdt(X),
+                                X.numel(), _ptr(Y), Y.numel(), M, K, N, _stream(stream)), "qgemm_noalloc")
     return Y
 
 

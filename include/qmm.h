@@ -88,7 +88,8 @@ typedef enum {
     QMM_ERR_UNIMPLEMENTED = 12,
     QMM_ERR_BAD_ARGUMENT = 13,           /* negative size or other bad scalar */
     QMM_ERR_OUTPUT_TOO_SMALL = 14,       /* y_elems < outputs to write */
-    QMM_ERR_WORKSPACE_IN_CAPTURE = 15    /* workspace would grow during stream capture */
+    QMM_ERR_WORKSPACE_IN_CAPTURE = 15,   /* workspace would grow during stream capture */
+    QMM_ERR_NOALLOC_LIMIT = 16           /* qgemm_noalloc: scratch needed exceeds its fixed array */
 } qmm_status;
 
 /* Geometry of `kind`: bytes and elements of one block. Returns QMM_OK or
@@ -160,6 +161,33 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
  */
 QMM_API int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
           float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream);
+
+/*
+ * qgemm_noalloc -- qgemm on the tensor-core path that never allocates device
+ * memory. No passage of the pages has a counterpart: this entry point exists
+ * for callers that cannot let a library call cudaMalloc -- code running while
+ * its stream is being captured into a CUDA graph (an allocation there breaks
+ * the capture), and runtimes that reserve all device memory up front and
+ * hand out only their own pools.
+ *
+ * It computes exactly what qgemm computes, with the same arguments, layouts
+ * and accuracy, but only on the tensor-core path: f16 activations, K a
+ * multiple of 256, 16-byte aligned W and X, rows a multiple of 16 bytes
+ * (QMM_ERR_UNIMPLEMENTED otherwise). The per-group activation sums that
+ * Q4_K, Q5_K and Q2_K need go to a fixed 4 MiB device array compiled into the
+ * library (held on every GPU that loads it, until the process exits) instead
+ * of a grown workspace; a problem whose sums need more,
+ * N * (K / 256) * 32 bytes for Q4_K / Q5_K or N * (K / 256) * 64 bytes for
+ * Q2_K above 4 MiB, returns QMM_ERR_NOALLOC_LIMIT before anything is launched.
+ * Each call rewrites all the scratch it reads. The array is shared by every
+ * call: calls that can overlap on the GPU (different streams, same device)
+ * race on it and must be ordered by the caller. The first call on a device
+ * looks the array's address up (cudaGetSymbolAddress, no allocation); make
+ * that first call before any stream capture.
+ */
+QMM_API int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype,
+                          size_t x_elems, float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N,
+                          void* stream);
 
 /*
  * qgemm_grouped -- expert-indexed product (a mixture-of-experts layer's

@@ -39,7 +39,7 @@ def test_kind_table(L):
 
 
 def test_status_strings(L):
-    for code in range(16):
+    for code in range(17):
         assert L.qmm_status_str(code)
     assert L.qmm_status_str(999) == b"unknown status"
 
