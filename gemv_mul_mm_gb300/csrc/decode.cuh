@@ -170,57 +170,8 @@ template <int KIND> struct TcGeo {
     static constexpr int MIN_GROUPS = KIND == Q2_K ? 16 : 8;                 // min groups per 256
 };
 
-// Code of element i (0..31) of 32-element chunk j of the block at b.
-template <int KIND>
-__device__ __forceinline__ float code32(const uint8_t* b, int j, int i) {
-    if constexpr (KIND == Q8_0) {
-        return static_cast<float>(static_cast<int8_t>(b[2 + i]));
-    } else if constexpr (KIND == Q4_0 || KIND == IQ4_NL) {
-        const uint32_t byte = b[2 + (i & 15)];
-        const int c = (i < 16) ? (byte & 15) : (byte >> 4);
-        if constexpr (KIND == Q4_0) return static_cast<float>(c - 8);
-        else return c_kv_iq4nl[c];
-    } else if constexpr (KIND == Q5_0) {
-        const uint32_t qh = ld8(b, 2) | (ld8(b, 3) << 8) | (ld8(b, 4) << 16) | (ld8(b, 5) << 24);
-        const uint32_t byte = b[6 + (i & 15)];
-        const int lo = (i < 16) ? (byte & 15) : (byte >> 4);
-        const int q = lo | static_cast<int>(((qh >> i) & 1) << 4);
-        return static_cast<float>(q - 16);
-    } else if constexpr (KIND == MXFP4) {
-        const uint32_t byte = b[1 + (i & 15)];
-        return c_kv_e2m1[(i < 16) ? (byte & 15) : (byte >> 4)];
-    } else if constexpr (KIND == Q4_K || KIND == Q5_K) {
-        int sc, mn;
-        k4_sm(b + 4, j, sc, mn);
-        const int qs = (KIND == Q4_K) ? 16 : 48;
-        const uint32_t byte = b[qs + (j >> 1) * 32 + i];
-        int q = (j & 1) ? (byte >> 4) : (byte & 15);
-        if constexpr (KIND == Q5_K) q += ((b[16 + i] >> j) & 1) << 4;
-        return static_cast<float>(sc * q);
-    } else if constexpr (KIND == Q6_K) {
-        const int h = j >> 2, g = j & 3;
-        const uint32_t lob = b[h * 64 + i + (g & 1) * 32];
-        const int lo = (g >= 2) ? (lob >> 4) : (lob & 15);
-        const int hi = (b[128 + h * 32 + i] >> (2 * g)) & 3;
-        const int sc = static_cast<int8_t>(b[192 + 2 * j + (i >> 4)]);
-        return static_cast<float>(sc * ((lo | (hi << 4)) - 32));
-    } else if constexpr (KIND == Q2_K) {
-        const int h = j >> 2, g = j & 3;
-        const int q = (b[16 + h * 32 + i] >> (2 * g)) & 3;
-        return static_cast<float>((b[2 * j + (i >> 4)] & 15) * q);
-    } else if constexpr (KIND == Q3_K) {
-        const int h = j >> 2, g = j & 3;
-        const int q2 = (b[32 + h * 32 + i] >> (2 * g)) & 3;
-        const int q = q2 - (((b[i] >> j) & 1) ? 0 : 4);
-        return static_cast<float>((q3_scale(b + 96, 2 * j + (i >> 4)) - 32) * q);
-    } else {  // IQ4_XS
-        const uint32_t byte = b[8 + 16 * j + (i & 15)];
-        const int c = (i < 16) ? (byte & 15) : (byte >> 4);
-        const uint32_t sh = ld16(b, 2);
-        const int ls = ((b[4 + (j >> 1)] >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4);
-        return static_cast<float>(ls - 32) * c_kv_iq4nl[c];
-    }
-}
+// The codes themselves are produced per sub-step, in registers, by the fast
+// decoders of tc_fastdec.cuh.
 
 // fp32 scale of a 32-element block (PER32 formats).
 template <int KIND>

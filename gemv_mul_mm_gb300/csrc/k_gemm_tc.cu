@@ -35,18 +35,22 @@
 #include "decode.cuh"
 #include "qmm_internal.cuh"
 #include "sm100_async.cuh"
+#include "tc_fastdec.cuh"
 
 namespace qmm {
 namespace {
 
 constexpr int BM = 128, BN = 128, KSUP = 256, KSUB = 64;
-constexpr int AS = 3, XS = 3, RS = 2;
 constexpr int kProdWarp = 0, kMmaWarp = 1, kDec0 = 2, kNumDec = 4, kEpi0 = 6, kNumEpi = 8;
-constexpr int kThreads = (kEpi0 + kNumEpi) * 32;  // 448
+constexpr int kXWarp = kEpi0 + kNumEpi;           // activation-tile producer
+constexpr int kThreads = (kXWarp + 1) * 32;       // 480
 constexpr int A_TILE = BM * KSUB * 2;             // 16 KB, 128B-swizzled K-major
 constexpr int X_TILE = BN * KSUB * 2;             // 16 KB
 constexpr int MIN_TILE = 128 * 32;                // 4 KB, 32B-swizzled K-major (K = 16)
 constexpr int kTmemCols = 512;
+// TMEM accumulator buffers: four 128-column units per 32-element block for the
+// per-32 formats, two (D1 | D2) pairs of 128 + 128 columns per super-block otherwise
+template <int KIND> struct NDBuf { static constexpr int N = TcGeo<KIND>::PER32 ? 4 : 2; };
 // instruction descriptor: D f32, A/B f16, both K-major, N = 128, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
 
@@ -59,6 +63,24 @@ template <int KIND> struct Raw {
     static constexpr int BOXB = ((B0 / 16) % 2 == 1) ? B0 : B0 + 16;    // odd number of 16-B lines per row
     static constexpr int STAGE = BM * BOXB;
     static_assert(BOXB / 2 <= 256, "TMA box inner dimension");
+};
+
+template <int KIND> struct Mins;
+
+// Pipeline depths per format: A stages (decoded codes), X stages (activation
+// sub-tiles), raw stages (quantized bytes per super-step), as deep as the
+// 227 KB of shared memory allow -- TMA latency must be covered by stages in
+// flight, while the A stages are produced locally.
+template <int KIND> struct Stages {
+    static constexpr int RAWB = 128 * Raw<KIND>::BOXB;
+    static constexpr int MINS = Mins<KIND>::TILES * 4096 * 4;   // amin + bmin, double buffered
+    static constexpr int FIXED = MINS + 2 * 128 * 8 * 4 + 2048 + 1024;
+    static constexpr int BUDGET = 226 * 1024 - FIXED;
+    static constexpr int AS = 4;
+    static constexpr int RS = (BUDGET - AS * 16384 - 5 * 16384) >= 3 * RAWB ? 3 : 2;
+    static constexpr int XS0 = (BUDGET - AS * 16384 - RS * RAWB) / 16384;
+    static constexpr int XS = XS0 > 8 ? 8 : XS0;
+    static_assert(XS >= 4, "shared memory for at least four activation stages");
 };
 
 template <int KIND> struct Mins {
@@ -144,6 +166,7 @@ template <int KIND>
 struct Layout {
     using R = Raw<KIND>;
     using MN = Mins<KIND>;
+    static constexpr int AS = Stages<KIND>::AS, XS = Stages<KIND>::XS, RS = Stages<KIND>::RS;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_X = OFF_A + AS * A_TILE;
     static constexpr int OFF_RAW = OFF_X + XS * X_TILE;
@@ -153,8 +176,8 @@ struct Layout {
     static constexpr int OFF_SC = OFF_BMIN + 2 * MINB;               // [2][128][8] floats
     static constexpr int OFF_BAR = OFF_SC + 2 * BM * 8 * 4;
     // barriers: raw_full/empty[RS], a_full/empty[AS], x_full/empty[XS], amin_full/empty[2],
-    // bmin_full/empty[2], d_full/empty[2], sc_full/empty[2], done
-    static constexpr int NBAR = 2 * RS + 2 * AS + 2 * XS + 4 + 4 + 4 + 4 + 1;
+    // bmin_full/empty[2], d_full/empty[ND], sc_full/empty[2], done
+    static constexpr int NBAR = 2 * RS + 2 * AS + 2 * XS + 4 + 4 + 2 * NDBuf<KIND>::N + 4 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16 + 1024;               // + alignment slack
 };
@@ -168,9 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = Layout<KIND>;
     constexpr bool PER32 = TcGeo<KIND>::PER32;
     constexpr int BB = Geo<KIND>::BB;
+    constexpr int AS = L::AS, XS = L::XS, RS = L::RS;
+    constexpr int ND = NDBuf<KIND>::N;
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived by pointer arithmetic on the shared array
+    // so that every access below compiles to shared (not generic) loads/stores
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* a_tiles = smem + L::OFF_A;
     uint8_t* x_tiles = smem + L::OFF_X;
     uint8_t* raw = smem + L::OFF_RAW;
@@ -189,8 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bmin_full = amin_empty + 2;
     uint64_t* bmin_empty = bmin_full + 2;
     uint64_t* d_full = bmin_empty + 2;
-    uint64_t* d_empty = d_full + 2;
-    uint64_t* sc_full = d_empty + 2;
+    uint64_t* d_empty = d_full + ND;
+    uint64_t* sc_full = d_empty + ND;
     uint64_t* sc_empty = sc_full + 2;
     uint64_t* done = sc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
@@ -213,13 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&x_full[i], 1);
             mbar_init(&x_empty[i], 1);
         }
+        for (int i = 0; i < ND; ++i) {
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kNumEpi);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&amin_full[i], kNumDec);
             mbar_init(&amin_empty[i], 1);
             mbar_init(&bmin_full[i], 1);
             mbar_init(&bmin_empty[i], 1);
-            mbar_init(&d_full[i], 1);
-            mbar_init(&d_empty[i], kNumEpi);
             mbar_init(&sc_full[i], kNumDec);
             mbar_init(&sc_empty[i], kNumEpi);
         }
@@ -239,9 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kProdWarp) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer: weights (+ group sums)
         if (lane == 0) {
-            int sx = 0;  // X sub-steps issued
             int s_issued = 0;
             for (int s = 0; s < nsup; ++s) {
                 const int rs = s % RS;
@@ -250,30 +278,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma2d(raw + rs * R::STAGE, &tmW, ((s * R::SBB) & ~15) / 2, m0, &raw_full[rs]);
                 if constexpr (MN::ON) {
                     const int b = s & 1;
-                    if (s >= 2 && !wait_bar(&bmin_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err)) break;
+                    if (s >= 2 && !wait_bar(&bmin_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err)) {
+                        s_issued = s + 1;
+                        break;
+                    }
                     mbar_arrive_expect_tx(&bmin_full[b], L::MINB);
 #pragma unroll
                     for (int t = 0; t < MN::TILES; ++t)
                         tma2d(bmin + b * L::MINB + t * MIN_TILE, &tmB, s * MN::KMW + 16 * t, n0, &bmin_full[b]);
                 }
                 s_issued = s + 1;
-                bool ok = true;
-                for (int q = 0; q < KSUP / KSUB; ++q, ++sx) {
-                    const int xs = sx % XS;
-                    if (sx >= XS && !wait_bar(&x_empty[xs], ((sx / XS) - 1) & 1, abort_flag, a.err)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&x_full[xs], X_TILE);
-                    tma2d(x_tiles + xs * X_TILE, &tmX, s * KSUP + q * KSUB, n0, &x_full[xs]);
-                }
-                if (!ok) break;
             }
             // every issued copy must land before the CTA retires
-            for (int s = (s_issued > RS ? s_issued - RS : 0); s < s_issued; ++s) drain_bar(&raw_full[s % RS], (s / RS) & 1, a.err);
-            for (int i = (sx > XS ? sx - XS : 0); i < sx; ++i) drain_bar(&x_full[i % XS], (i / XS) & 1, a.err);
+            for (int s = (s_issued > RS ? s_issued - RS : 0); s < s_issued; ++s)
+                drain_bar(&raw_full[s % RS], (s / RS) & 1, a.err);
             if constexpr (MN::ON)
-                for (int s = (s_issued > 2 ? s_issued - 2 : 0); s < s_issued; ++s) drain_bar(&bmin_full[s & 1], (s >> 1) & 1, a.err);
+                for (int s = (s_issued > 2 ? s_issued - 2 : 0); s < s_issued; ++s)
+                    drain_bar(&bmin_full[s & 1], (s >> 1) & 1, a.err);
+        }
+    } else if (warp == kXWarp) {
+        // ------------------------------------------------ TMA producer: activation sub-tiles
+        if (lane == 0) {
+            int sx = 0;
+            const int nsub = nsup * (KSUP / KSUB);
+            for (; sx < nsub; ++sx) {
+                const int xs = sx % XS;
+                if (sx >= XS && !wait_bar(&x_empty[xs], ((sx / XS) - 1) & 1, abort_flag, a.err)) break;
+                mbar_arrive_expect_tx(&x_full[xs], X_TILE);
+                tma2d(x_tiles + xs * X_TILE, &tmX, sx * KSUB, n0, &x_full[xs]);
+            }
+            for (int i = (sx > XS ? sx - XS : 0); i < sx; ++i) drain_bar(&x_full[i % XS], (i / XS) & 1, a.err);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -290,9 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < KSUB / 16; ++kk) {
                         if constexpr (PER32) {
-                            const int u = 8 * s + 2 * q + (kk >> 1), b = u & 1;
-                            if ((kk & 1) == 0 && u >= 2) {
-                                if (!wait_bar(&d_empty[b], ((u >> 1) - 1) & 1, abort_flag, a.err)) break;
+                            const int u = 8 * s + 2 * q + (kk >> 1), b = u % ND;
+                            if ((kk & 1) == 0 && u >= ND) {
+                                if (!wait_bar(&d_empty[b], ((u / ND) - 1) & 1, abort_flag, a.err)) break;
                                 tc_fence_after();
                             }
                             tc_mma(tmem + b * BN, desc_sw128(abase + 32 * kk), desc_sw128(xbase + 32 * kk), kIdesc,
@@ -383,26 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && sub >= AS) ok = wait_bar(&a_empty[as], ((sub / AS) - 1) & 1, abort_flag, a.err);
                 if (ok) {
                     uint8_t* base = a_tiles + as * A_TILE + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll 2
-                    for (int c = 0; c < 8; ++c) {
-                        const int e0 = q * KSUB + c * 8;  // element within the super-step
-                        uint32_t w[4];
+                    uint32_t o[32];
+                    FastDec<KIND>::sub(row, q, o);
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const int e = e0 + 2 * t;
-                            float v0, v1;
-                            if constexpr (PER32) {
-                                const uint8_t* b = row + (e >> 5) * BB;
-                                v0 = code32<KIND>(b, 0, e & 31);
-                                v1 = code32<KIND>(b, 0, (e + 1) & 31);
-                            } else {
-                                v0 = code32<KIND>(row, e >> 5, e & 31);
-                                v1 = code32<KIND>(row, e >> 5, (e + 1) & 31);
-                            }
-                            w[t] = pack_h2(v0, v1);
-                        }
-                        *reinterpret_cast<uint4*>(base + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(base + ((c ^ (r & 7)) << 4)) =
+                            make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
                     fence_proxy_async();
                 }
                 __syncwarp();
@@ -418,26 +438,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = ew >> 2;                  // column half: 64 columns each
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        float acc[64];
+        float2 acc[32];   // columns 2i, 2i + 1 of this thread's 64, updated with packed FMAs
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+        for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
         for (int s = 0; s < nsup; ++s) {
             const float* sc = sbuf + ((s & 1) * BM + r) * 8;
             wait_bar(&sc_full[s & 1], (s >> 1) & 1, abort_flag, a.err);
             if constexpr (PER32) {
                 for (int j = 0; j < 8; ++j) {
-                    const int u = 8 * s + j, b = u & 1;
-                    const bool ok = wait_bar(&d_full[b], (u >> 1) & 1, abort_flag, a.err);
+                    const int u = 8 * s + j, b = u % ND;
+                    const bool ok = wait_bar(&d_full[b], (u / ND) & 1, abort_flag, a.err);
                     tc_fence_after();
-                    const float d = sc[j];
+                    const float2 d2 = make_float2(sc[j], sc[j]);
                     if (ok) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            float v[16];
-                            tmem_ld16(tmem + lane_addr + b * BN + half * 64 + c * 16, v);
+                        for (int c = 0; c < 4; c += 2) {
+                            float v[32];
+                            tmem_ld16(tmem + lane_addr + b * BN + half * 64 + c * 16, *reinterpret_cast<float(*)[16]>(v));
+                            tmem_ld16(tmem + lane_addr + b * BN + half * 64 + c * 16 + 16,
+                                      *reinterpret_cast<float(*)[16]>(v + 16));
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(d, v[i], acc[c * 16 + i]);
+                            for (int i = 0; i < 16; ++i)
+                                acc[c * 8 + i] = __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]), acc[c * 8 + i]);
                         }
                     }
                     tc_fence_before();
@@ -448,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = s & 1;
                 const bool ok = wait_bar(&d_full[b], (s >> 1) & 1, abort_flag, a.err);
                 tc_fence_after();
-                const float d = sc[0], dm = sc[1];
+                const float2 d2 = make_float2(sc[0], sc[0]), ndm2 = make_float2(-sc[1], -sc[1]);
                 if (ok) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -459,12 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_ld16(tmem + lane_addr + b * 2 * BN + BN + half * 64 + c * 16, w2);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                acc[c * 16 + i] = fmaf(-dm, w2[i], fmaf(d, v[i], acc[c * 16 + i]));
+                            for (int i = 0; i < 8; ++i)
+                                acc[c * 8 + i] = __ffma2_rn(ndm2, make_float2(w2[2 * i], w2[2 * i + 1]),
+                                                            __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]),
+                                                                       acc[c * 8 + i]));
                         } else {
                             tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(d, v[i], acc[c * 16 + i]);
+                            for (int i = 0; i < 8; ++i)
+                                acc[c * 8 + i] = __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]), acc[c * 8 + i]);
                         }
                     }
                 }
@@ -480,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 const int n = n0 + half * 64 + i;
-                if (n < a.N) a.Y[static_cast<int64_t>(n) * a.M + m] = acc[i];
+                if (n < a.N) a.Y[static_cast<int64_t>(n) * a.M + m] = (i & 1) ? acc[i >> 1].y : acc[i >> 1].x;
             }
         }
     }

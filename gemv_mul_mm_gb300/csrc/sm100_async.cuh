@@ -44,14 +44,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint (ns): the thread may sleep up to that
+// long inside the instruction, and wakes when the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of `bar` with the given parity. `abort` is a
 // shared flag any warp may raise; waiting stops when it is set. Returns false
 // on timeout or abort (the timeout is latched into *err and raises *abort).
+// The abort flag and the clock are checked every 16 tries only.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
         if (*abort) return false;
         if (clock64() - t0 > (1ll << 31)) {  // ~1 s at 2 GHz
             atomicOr(err, DEV_ERR_TIMEOUT);
