@@ -5,22 +5,24 @@
 // as an fp32 FMA over shared tiles; here the contraction runs on tcgen05).
 //
 // One CTA computes a 128 (weight rows) x 128 (tokens) tile of Y:
-//   * warp 0 (one thread) issues the TMA loads: the raw quantized bytes of the
-//     tile's 128 rows for one 256-element super-step (a 2-D tensor map over W,
-//     16-byte aligned box), the f16 activation sub-tiles (128 tokens x 64 k,
-//     128-byte swizzled, exactly the K-major layout the MMA descriptor reads),
-//     and, for the formats with mins, the per-group activation sums.
-//   * warps 2-5 (one thread per weight row) decode the raw bytes into f16
-//     INTEGER CODES -- the stored code times its integer sub-scale, or the
-//     codebook value -- written to shared memory in the same swizzled
-//     K-major layout, plus the fp32 scales of the row;
-//   * warp 1 (one elected thread) issues tcgen05.mma kind::f16 (A = codes,
-//     B = activations, both from shared memory) into fp32 TMEM accumulators,
-//     one fresh accumulator per promotion unit, double buffered;
+//   * warp 0 (one thread) issues the TMA loads of the raw quantized bytes of
+//     the tile's 128 rows for one 256-element super-step (a 2-D tensor map over
+//     W, 16-byte aligned box) and, for the formats with mins, of the per-group
+//     activation sums; warp 14 (one thread) loads the f16 activation sub-tiles
+//     (128 tokens x 64 k, 128-byte swizzled, the K-major layout the MMA reads);
+//   * warps 2-5 (one thread per weight row) decode the raw bytes in registers
+//     into f16 INTEGER CODES -- the stored code times its integer sub-scale, or
+//     the codebook value -- and store them straight into tensor memory (the
+//     row's TMEM lane), plus the fp32 scales of the row into shared memory;
+//   * warp 1 (one elected thread) issues tcgen05.mma kind::f16 with A = codes
+//     from TMEM and B = activations from shared memory into fp32 TMEM
+//     accumulators, one fresh accumulator per promotion unit;
 //   * warps 6-13 read each finished unit from TMEM (tcgen05.ld) and apply the
 //     fp32 scales to the PARTIAL SUMS: acc += d * D1 - dmin * D2 per 256-element
 //     super-block (K-quants, IQ4_XS) or acc += d * D per 32-element block
 //     (Q8_0, Q4_0, Q5_0, IQ4_NL, MXFP4), then store Y.
+// Keeping A in TMEM halves the shared-memory traffic per MMA (only B is read
+// from shared memory) and spares the decoders the swizzled stores.
 // The K-quant mins (-dmin * sum_s m_s * sum_{k in s} x_k) come out of a second,
 // K = 16 (or 32) MMA per super-block: A = the integer mins, B = the per-group
 // activation sums split hi + lo in f16 (a pre-pass kernel), into accumulator D2.
@@ -41,16 +43,24 @@ namespace qmm {
 namespace {
 
 constexpr int BM = 128, BN = 128, KSUP = 256, KSUB = 64;
-constexpr int kProdWarp = 0, kMmaWarp = 1, kDec0 = 2, kNumDec = 4, kEpi0 = 6, kNumEpi = 8;
+constexpr int kProdWarp = 0, kMmaWarp = 1, kNumDec = 4, kEpi0 = 6, kNumEpi = 8;   // decoders: warps 2-5
 constexpr int kXWarp = kEpi0 + kNumEpi;           // activation-tile producer
-constexpr int kThreads = (kXWarp + 1) * 32;       // 480
-constexpr int A_TILE = BM * KSUB * 2;             // 16 KB, 128B-swizzled K-major
-constexpr int X_TILE = BN * KSUB * 2;             // 16 KB
+constexpr int kWaitWarp = kXWarp + 1;             // waits on behalf of the MMA issuer
+constexpr int kThreads = (kWaitWarp + 1) * 32;    // 512
+constexpr int kBarHand = 1;                       // named barriers 1, 2: waiter -> issuer hand-over
+constexpr int X_SUB = BN * KSUB * 2;              // 16 KB: one 64-wide activation sub-tile
+constexpr int X_TILE = 2 * X_SUB;                 // an activation stage holds two sub-steps
 constexpr int MIN_TILE = 128 * 32;                // 4 KB, 32B-swizzled K-major (K = 16)
 constexpr int kTmemCols = 512;
-// TMEM accumulator buffers: four 128-column units per 32-element block for the
-// per-32 formats, two (D1 | D2) pairs of 128 + 128 columns per super-block otherwise
-template <int KIND> struct NDBuf { static constexpr int N = TcGeo<KIND>::PER32 ? 4 : 2; };
+// Tensor memory (512 columns x 128 lanes, lane = weight row of the tile):
+//   [0, 128)    A operand: four stages of 64 f16 codes per row (32 columns each)
+//   [128, 512)  fp32 accumulators: three 128-column units, one per 32-element
+//               block, for the per-32 formats; otherwise D1 of two super-blocks
+//               (double buffered) at 128 and 256, and the min term D2 at 384.
+constexpr int kAStages = 4;
+constexpr int kACols = KSUB / 2;
+constexpr int kDCol0 = kAStages * kACols;
+template <int KIND> struct NDBuf { static constexpr int N = TcGeo<KIND>::PER32 ? 3 : 2; };
 // instruction descriptor: D f32, A/B f16, both K-major, N = 128, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
 
@@ -67,20 +77,20 @@ template <int KIND> struct Raw {
 
 template <int KIND> struct Mins;
 
-// Pipeline depths per format: A stages (decoded codes), X stages (activation
-// sub-tiles), raw stages (quantized bytes per super-step), as deep as the
-// 227 KB of shared memory allow -- TMA latency must be covered by stages in
-// flight, while the A stages are produced locally.
+// Shared-memory pipeline depths per format: X stages (activation sub-tiles) and
+// raw stages (quantized bytes per super-step), as deep as the 227 KB allow --
+// TMA latency must be covered by the stages in flight. (The decoded A stages
+// live in tensor memory.)
 template <int KIND> struct Stages {
     static constexpr int RAWB = 128 * Raw<KIND>::BOXB;
     static constexpr int MINS = Mins<KIND>::TILES * 4096 * 4;   // amin + bmin, double buffered
     static constexpr int FIXED = MINS + 2 * 128 * 8 * 4 + 2048 + 1024;
     static constexpr int BUDGET = 226 * 1024 - FIXED;
-    static constexpr int AS = 4;
-    static constexpr int RS = (BUDGET - AS * 16384 - 5 * 16384) >= 3 * RAWB ? 3 : 2;
-    static constexpr int XS0 = (BUDGET - AS * 16384 - RS * RAWB) / 16384;
-    static constexpr int XS = XS0 > 8 ? 8 : XS0;
-    static_assert(XS >= 4, "shared memory for at least four activation stages");
+    static constexpr int AS = kAStages;
+    static constexpr int RS = (BUDGET - 3 * X_TILE) >= 4 * RAWB ? 4 : (BUDGET - 3 * X_TILE) >= 3 * RAWB ? 3 : 2;
+    static constexpr int XS0 = (BUDGET - RS * RAWB) / X_TILE;
+    static constexpr int XS = XS0 > 4 ? 4 : XS0;
+    static_assert(XS >= 3, "shared memory for at least three activation stages");
 };
 
 template <int KIND> struct Mins {
@@ -139,6 +149,38 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// A operand from tensor memory, B from shared memory
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// 32 consecutive 32-bit columns of this thread's lane
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+        "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+        "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+// Named-barrier rendezvous of `nthreads` threads (whole warps) that also
+// returns the AND of every participant's `v`.
+__device__ __forceinline__ bool bar_red_and(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+        "bar.red.and.pred q, %1, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(static_cast<uint32_t>(v)), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
@@ -146,9 +188,31 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 
 // Bounded wait that also honours the CTA's abort flag; false = give up.
+// A phase that has already completed is taken without touching the flag.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+    if (mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
     return mbar_wait(bar, parity, abort, err);
+}
+
+// Polling variant for the waits on the critical path of the pipeline.
+__device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+    return mbar_wait_poll(bar, parity, abort, err, 32u);
+}
+
+// The same for a whole warp: lane 0 alone polls the barrier (hundreds of
+// polling lanes slow down every other barrier operation of the CTA, among
+// them the MMA issuer's), __syncwarp orders the other lanes after its
+// acquire, and the outcome is broadcast. All 32 lanes must call it.
+template <bool SPIN = false>
+__device__ __forceinline__ bool warp_wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0)
+        ok = (SPIN ? spin_bar(bar, parity, abort, err) : wait_bar(bar, parity, abort, err)) ? 1 : 0;
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Waits (bounded, ignoring abort) for the phase with `parity` of a barrier.
@@ -167,8 +231,7 @@ struct Layout {
     using R = Raw<KIND>;
     using MN = Mins<KIND>;
     static constexpr int AS = Stages<KIND>::AS, XS = Stages<KIND>::XS, RS = Stages<KIND>::RS;
-    static constexpr int OFF_A = 0;
-    static constexpr int OFF_X = OFF_A + AS * A_TILE;
+    static constexpr int OFF_X = 0;
     static constexpr int OFF_RAW = OFF_X + XS * X_TILE;
     static constexpr int OFF_AMIN = (OFF_RAW + RS * R::STAGE + 1023) & ~1023;
     static constexpr int MINB = MN::TILES * MIN_TILE;
@@ -198,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte aligned base, derived by pointer arithmetic on the shared array
     // so that every access below compiles to shared (not generic) loads/stores
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* a_tiles = smem + L::OFF_A;
     uint8_t* x_tiles = smem + L::OFF_X;
     uint8_t* raw = smem + L::OFF_RAW;
     uint8_t* amin = smem + L::OFF_AMIN;
@@ -300,82 +362,119 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ TMA producer: activation sub-tiles
         if (lane == 0) {
             int sx = 0;
-            const int nsub = nsup * (KSUP / KSUB);
-            for (; sx < nsub; ++sx) {
+            const int nx = nsup * (KSUP / KSUB) / 2;   // stages of two sub-steps
+            for (; sx < nx; ++sx) {
                 const int xs = sx % XS;
                 if (sx >= XS && !wait_bar(&x_empty[xs], ((sx / XS) - 1) & 1, abort_flag, a.err)) break;
                 mbar_arrive_expect_tx(&x_full[xs], X_TILE);
-                tma2d(x_tiles + xs * X_TILE, &tmX, sx * KSUB, n0, &x_full[xs]);
+                tma2d(x_tiles + xs * X_TILE, &tmX, 2 * sx * KSUB, n0, &x_full[xs]);
+                tma2d(x_tiles + xs * X_TILE + X_SUB, &tmX, (2 * sx + 1) * KSUB, n0, &x_full[xs]);
             }
             for (int i = (sx > XS ? sx - XS : 0); i < sx; ++i) drain_bar(&x_full[i % XS], (i / XS) & 1, a.err);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int sub = 0;
-            for (int s = 0; s < nsup && !*abort_flag; ++s) {
-                for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
-                    const int as = sub % AS, xs = sub % XS;
-                    if (!wait_bar(&a_full[as], (sub / AS) & 1, abort_flag, a.err)) break;
-                    if (!wait_bar(&x_full[xs], (sub / XS) & 1, abort_flag, a.err)) break;
+        // The warp follows the schedule converged and lane 0 issues. It never
+        // touches shared memory between MMAs (a shared-memory access queued
+        // behind MMAs stalls for ~100 cycles): the waits are done by the
+        // waiter warp, which hands each ready sub-step over through a named
+        // barrier (bar.red also carries whether to go on).
+        int sub = 0;
+        for (int s = 0; s < nsup; ++s) {
+            for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
+                const bool go = bar_red_and(kBarHand + (sub & 1), 64, true);
+                if (go && lane == 0) {
                     tc_fence_after();
-                    const uint32_t abase = smem_u32(a_tiles + as * A_TILE);
-                    const uint32_t xbase = smem_u32(x_tiles + xs * X_TILE);
+                    const int as = sub % AS, xs = (sub >> 1) % XS;
+                    const uint32_t a_tm = tmem + as * kACols;
+                    const uint32_t xbase = smem_u32(x_tiles + xs * X_TILE + (sub & 1) * X_SUB);
 #pragma unroll
                     for (int kk = 0; kk < KSUB / 16; ++kk) {
                         if constexpr (PER32) {
-                            const int u = 8 * s + 2 * q + (kk >> 1), b = u % ND;
-                            if ((kk & 1) == 0 && u >= ND) {
-                                if (!wait_bar(&d_empty[b], ((u / ND) - 1) & 1, abort_flag, a.err)) break;
-                                tc_fence_after();
-                            }
-                            tc_mma(tmem + b * BN, desc_sw128(abase + 32 * kk), desc_sw128(xbase + 32 * kk), kIdesc,
-                                   kk & 1);
+                            const int b = (8 * s + 2 * q + (kk >> 1)) % ND;
+                            tc_mma_ts(tmem + kDCol0 + b * BN, a_tm + 8 * kk, desc_sw128(xbase + 32 * kk), kIdesc,
+                                      kk & 1);
                             if (kk & 1) tc_commit(&d_full[b]);
                         } else {
-                            const int b = s & 1;
-                            if (q == 0 && kk == 0 && s >= 2) {
-                                if (!wait_bar(&d_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err)) break;
-                                tc_fence_after();
-                            }
-                            tc_mma(tmem + b * 2 * BN, desc_sw128(abase + 32 * kk), desc_sw128(xbase + 32 * kk), kIdesc,
-                                   (q | kk) != 0);
+                            tc_mma_ts(tmem + kDCol0 + (s & 1) * BN, a_tm + 8 * kk, desc_sw128(xbase + 32 * kk),
+                                      kIdesc, (q | kk) != 0);
                         }
                     }
                     tc_commit(&a_empty[as]);
-                    tc_commit(&x_empty[xs]);
-                }
-                if constexpr (!PER32) {
-                    const int b = s & 1;
-                    if constexpr (MN::ON) {
-                        if (!wait_bar(&amin_full[b], (s >> 1) & 1, abort_flag, a.err)) break;
-                        if (!wait_bar(&bmin_full[b], (s >> 1) & 1, abort_flag, a.err)) break;
-                        tc_fence_after();
+                    if (sub & 1) tc_commit(&x_empty[xs]);
+                    if constexpr (!PER32) {
+                        if (q == KSUP / KSUB - 1) {
+                            const int b = s & 1;
+                            if constexpr (MN::ON) {
 #pragma unroll
-                        for (int t = 0; t < MN::TILES; ++t)
-                            tc_mma(tmem + b * 2 * BN + BN, desc_sw32(smem_u32(amin + b * L::MINB + t * MIN_TILE)),
-                                   desc_sw32(smem_u32(bmin + b * L::MINB + t * MIN_TILE)), kIdesc, t);
-                        tc_commit(&amin_empty[b]);
-                        tc_commit(&bmin_empty[b]);
+                                for (int t = 0; t < MN::TILES; ++t)
+                                    tc_mma(tmem + kDCol0 + 2 * BN,
+                                           desc_sw32(smem_u32(amin + b * L::MINB + t * MIN_TILE)),
+                                           desc_sw32(smem_u32(bmin + b * L::MINB + t * MIN_TILE)), kIdesc, t);
+                                tc_commit(&amin_empty[b]);
+                                tc_commit(&bmin_empty[b]);
+                            }
+                            tc_commit(&d_full[b]);
+                        }
                     }
-                    tc_commit(&d_full[b]);
                 }
+                __syncwarp();
             }
+        }
+        if (lane == 0) {
             // all MMAs issued by this thread are complete before TMEM is freed
             tc_commit(done);
             drain_bar(done, 0, a.err);
         }
         __syncwarp();
+    } else if (warp == kWaitWarp) {
+        // ------------------------------------------------------------ MMA waiter
+        // Waits (lane 0, bounded) for everything sub-step `sub` needs -- its A
+        // stage, its activation stage, free accumulators and, at the end of a
+        // super-block, the mins tiles -- then releases it to the issuer. After
+        // a failure it keeps handing over "stop" so both sides stay in step.
+        int sub = 0;
+        bool ok = true;
+        for (int s = 0; s < nsup; ++s) {
+            for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
+                if (lane == 0 && ok) {
+                    const int as = sub % AS, xi = sub >> 1, xs = xi % XS;
+                    ok = spin_bar(&a_full[as], (sub / AS) & 1, abort_flag, a.err);
+                    if (ok && (sub & 1) == 0) ok = spin_bar(&x_full[xs], (xi / XS) & 1, abort_flag, a.err);
+                    if constexpr (PER32) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int u = 8 * s + 2 * q + h;
+                            if (ok && u >= ND) ok = spin_bar(&d_empty[u % ND], ((u / ND) - 1) & 1, abort_flag, a.err);
+                        }
+                    } else {
+                        if (ok && q == 0 && s >= 2) ok = spin_bar(&d_empty[s & 1], ((s >> 1) - 1) & 1, abort_flag, a.err);
+                        if constexpr (MN::ON) {
+                            if (q == KSUP / KSUB - 1) {
+                                const int b = s & 1;
+                                if (ok) ok = spin_bar(&amin_full[b], (s >> 1) & 1, abort_flag, a.err);
+                                if (ok) ok = spin_bar(&bmin_full[b], (s >> 1) & 1, abort_flag, a.err);
+                                // D2 is single-buffered: the epilogue must be done with super-block s - 1
+                                if (ok && s >= 1) ok = spin_bar(&d_empty[(s - 1) & 1], ((s - 1) >> 1) & 1, abort_flag, a.err);
+                            }
+                        }
+                    }
+                }
+                bar_red_and(kBarHand + (sub & 1), 64, lane != 0 || ok);
+            }
+        }
     } else if (warp < kEpi0) {
         // ------------------------------------------------------------ decoders
-        const int r = (warp - kDec0) * 32 + lane;  // weight row within the tile
+        // weight row within the tile = the TMEM lane this warp may access
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
         int sub = 0;
         for (int s = 0; s < nsup; ++s) {
             const int rs = s % RS;
-            bool ok = wait_bar(&raw_full[rs], (s / RS) & 1, abort_flag, a.err);
+            bool ok = warp_wait_bar(&raw_full[rs], (s / RS) & 1, abort_flag, a.err);
             const uint8_t* row = raw + rs * R::STAGE + r * R::BOXB + ((s * R::SBB) & 15);
             // scales for the epilogue
-            if (ok && s >= 2) ok = wait_bar(&sc_empty[s & 1], ((s >> 1) - 1) & 1, abort_flag, a.err);
+            if (ok && s >= 2) ok = warp_wait_bar(&sc_empty[s & 1], ((s >> 1) - 1) & 1, abort_flag, a.err);
             float* sc = sbuf + ((s & 1) * BM + r) * 8;
             if (ok) {
                 if constexpr (PER32) {
@@ -391,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&sc_full[s & 1]);
             if constexpr (MN::ON) {
                 const int b = s & 1;
-                if (ok && s >= 2) ok = wait_bar(&amin_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err);
+                if (ok && s >= 2) ok = warp_wait_bar(&amin_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err);
                 if (ok) {
                     // A_min tile(s): 32B-swizzled K-major, 16 f16 per row per tile
 #pragma unroll
@@ -414,17 +513,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
                 const int as = sub % AS;
-                if (ok && sub >= AS) ok = wait_bar(&a_empty[as], ((sub / AS) - 1) & 1, abort_flag, a.err);
+                // decode first, then wait for the stage to be free: the decode
+                // stays off the stage's round trip (ok is warp-uniform:
+                // tcgen05.st below is warp-collective)
+                uint32_t o[32];
+                if (ok) FastDec<KIND>::sub(row, q, o);
+                if (ok && sub >= AS) ok = warp_wait_bar<true>(&a_empty[as], ((sub / AS) - 1) & 1, abort_flag, a.err);
                 if (ok) {
-                    uint8_t* base = a_tiles + as * A_TILE + (r >> 3) * 1024 + (r & 7) * 128;
-                    uint32_t o[32];
-                    FastDec<KIND>::sub(row, q, o);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(base + ((c ^ (r & 7)) << 4)) =
-                            make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-                    fence_proxy_async();
+                    tc_fence_after();
+                    tmem_st32(tmem + lane_addr + as * kACols, o);
+                    tmem_wait_st();
                 }
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[as]);
             }
@@ -443,19 +543,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
         for (int s = 0; s < nsup; ++s) {
             const float* sc = sbuf + ((s & 1) * BM + r) * 8;
-            wait_bar(&sc_full[s & 1], (s >> 1) & 1, abort_flag, a.err);
+            warp_wait_bar(&sc_full[s & 1], (s >> 1) & 1, abort_flag, a.err);
             if constexpr (PER32) {
                 for (int j = 0; j < 8; ++j) {
                     const int u = 8 * s + j, b = u % ND;
-                    const bool ok = wait_bar(&d_full[b], (u / ND) & 1, abort_flag, a.err);
+                    const bool ok = warp_wait_bar(&d_full[b], (u / ND) & 1, abort_flag, a.err);
                     tc_fence_after();
                     const float2 d2 = make_float2(sc[j], sc[j]);
                     if (ok) {
 #pragma unroll
                         for (int c = 0; c < 4; c += 2) {
                             float v[32];
-                            tmem_ld16(tmem + lane_addr + b * BN + half * 64 + c * 16, *reinterpret_cast<float(*)[16]>(v));
-                            tmem_ld16(tmem + lane_addr + b * BN + half * 64 + c * 16 + 16,
+                            tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16,
+                                      *reinterpret_cast<float(*)[16]>(v));
+                            tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16 + 16,
                                       *reinterpret_cast<float(*)[16]>(v + 16));
                             tmem_wait_ld();
 #pragma unroll
@@ -469,17 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 const int b = s & 1;
-                const bool ok = wait_bar(&d_full[b], (s >> 1) & 1, abort_flag, a.err);
+                const bool ok = warp_wait_bar(&d_full[b], (s >> 1) & 1, abort_flag, a.err);
                 tc_fence_after();
                 const float2 d2 = make_float2(sc[0], sc[0]), ndm2 = make_float2(-sc[1], -sc[1]);
                 if (ok) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         float v[16];
-                        tmem_ld16(tmem + lane_addr + b * 2 * BN + half * 64 + c * 16, v);
+                        tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16, v);
                         if constexpr (MN::ON) {
                             float w2[16];
-                            tmem_ld16(tmem + lane_addr + b * 2 * BN + BN + half * 64 + c * 16, w2);
+                            tmem_ld16(tmem + lane_addr + kDCol0 + 2 * BN + half * 64 + c * 16, w2);
                             tmem_wait_ld();
 #pragma unroll
                             for (int i = 0; i < 8; ++i)

@@ -44,6 +44,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe: true if the phase with the given parity has completed.
+// Much cheaper than try_wait when the phase is already complete.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // try_wait with a suspend-time hint (ns): the thread may sleep up to that
 // long inside the instruction, and wakes when the phase completes.
 __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
@@ -69,6 +83,28 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
             if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > (1ll << 31)) {  // ~1 s at 2 GHz
+            atomicOr(err, DEV_ERR_TIMEOUT);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// Bounded wait for waits on a pipeline's critical path: polls with the cheap
+// test_wait and naps `ns` nanoseconds between probes (a thread suspended in
+// try_wait wakes up late; a tight spin takes issue slots from busy warps).
+// The abort flag and the clock are checked every 16 probes.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err,
+                                               unsigned ns) {
+    const long long t0 = clock64();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            if (mbar_test_wait(bar, parity)) return true;
+            __nanosleep(ns);
+        }
         if (*abort) return false;
         if (clock64() - t0 > (1ll << 31)) {  // ~1 s at 2 GHz
             atomicOr(err, DEV_ERR_TIMEOUT);
