@@ -48,6 +48,11 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="skip the per-kind GEMM/MoE/dequant table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="run one workload --reps times, untimed, and exit (a target for ncu): "
+                         "gemv:<kind> (decode GEMV), gemm:<kind> (prefill GEMM of the kind's workload), "
+                         "moe:<gate_up|down>:<T>, dequant:<kind>")
+    ap.add_argument("--reps", type=int, default=3)
     return ap.parse_args()
 
 
@@ -487,8 +492,53 @@ def run_ours(a):
     d.close()
 
 
+def run_case(a):
+    """One workload, --reps back-to-back calls on one stream, no timing: the
+    launch an ncu capture selects with -k / -c."""
+    import torch
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from gemv_mul_mm_gb300 import qmm, synth
+    what, _, arg = a.case.partition(":")
+    if what == "gemv":
+        qmm.set_weight_prefetch(True)
+        c = synth.DECODE
+        W = torch.from_numpy(synth.workload_weights(c, arg)).cuda()
+        x = torch.from_numpy(synth.workload_x(c, arg)).cuda()
+        fn = lambda: qmm.qgemv(arg, W, x, c["M"], c["K"])
+    elif what == "gemm":
+        c = synth.KQUANT if arg in synth.KQUANT["kinds"] else synth.CODEBOOK
+        W = torch.from_numpy(synth.workload_weights(c, arg)).cuda()
+        X = torch.from_numpy(synth.workload_x(c, arg)).cuda()
+        fn = lambda: qmm.qgemm(arg, W, X, c["M"], c["K"], c["N"])
+    elif what == "moe":
+        which, _, T = arg.partition(":")
+        p = synth.moe_problem(int(T), which)
+        W, X = torch.from_numpy(p["w"]).cuda(), torch.from_numpy(p["x"]).cuda()
+        xr, eid = torch.from_numpy(p["x_row"]).cuda(), torch.from_numpy(p["expert_id"]).cuda()
+        fn = lambda: qmm.qgemm_grouped(p["kind"], W, p["stride"], p["n_experts"], X, xr, eid, p["M"], p["K"])
+    elif what == "dequant":
+        c = synth.DECODE if arg in ("Q8_0", "Q4_0") else (synth.KQUANT if arg in synth.KQUANT["kinds"]
+                                                           else synth.CODEBOOK)
+        W = torch.from_numpy(synth.workload_weights(c, arg)).cuda()
+        fn = lambda: qmm.qdequant(arg, W, c["M"], c["K"])
+    else:
+        raise SystemExit(f"unknown case {a.case!r}")
+    for _ in range(a.reps):
+        fn()
+    torch.cuda.synchronize()
+    rc = qmm.check_device_error()
+    print(json.dumps({"case": a.case, "reps": a.reps, "device_error": rc}))
+    if rc:
+        raise SystemExit(1)
+
+
 def main():
     a = parse()
+    if a.case:
+        run_case(a)
+        return
     if a.impl == "reference":
         run_reference(a)
     else:
