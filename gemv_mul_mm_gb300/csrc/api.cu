@@ -7,6 +7,8 @@
 #include "qmm.h"
 #include "qmm_internal.cuh"
 
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -81,6 +83,33 @@ int sm_count(int device) {
 }
 
 bool weight_prefetch() { return g_prefetch.load(std::memory_order_relaxed) != 0; }
+
+bool encode_tiled_map(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                      const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw,
+                      CUtensorMapL2promotion promo) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    return fn(tm, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, b, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, promo,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
@@ -247,7 +276,11 @@ int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert_stride,
     p.n_experts = n_experts;
     p.n_x_rows = n_x_rows;
     p.err = err;
-    return finish(launch_generic(p, static_cast<cudaStream_t>(stream)), 1);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // every touched expert's rows stream once on the GEMV kernel; shapes it
+    // does not take (unaligned rows, too many experts) run on the generic one
+    if (g_path.load() != 1 && gemv_stream_ok(p)) return finish(launch_gemv_stream(p, s), 2);
+    return finish(launch_generic(p, s), 1);
 }
 
 int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,

@@ -641,30 +641,12 @@ __global__ void k_xsums(const __half* __restrict__ X, int N, int K, int gsize, i
 }
 
 // ------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 bool make_map(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
               uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {dim0, dim1};
-    const cuuint64_t strides[1] = {stride1_bytes};
-    const cuuint32_t box[2] = {box0, box1};
-    const cuuint32_t es[2] = {1, 1};
-    return fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[2] = {dim0, dim1};
+    const uint64_t strides[1] = {stride1_bytes};
+    const uint32_t box[2] = {box0, box1};
+    return encode_tiled_map(tm, dt, 2, base, dims, strides, box, sw);
 }
 
 // Library-owned per-device workspace for the activation sums (grown on demand;
@@ -702,7 +684,7 @@ template <int KIND>
 void ok_kind(const Problem& p, bool* out) {
     *out = !p.x_row && p.x_dtype == 1 && p.K % KSUP == 0 && p.row_bytes % 16 == 0 &&
            reinterpret_cast<uintptr_t>(p.W) % 16 == 0 && reinterpret_cast<uintptr_t>(p.X) % 16 == 0 &&
-           p.M <= (int64_t(1) << 30) && p.N <= (int64_t(1) << 30) && p.K <= (int64_t(1) << 30) && encode_fn();
+           p.M <= (int64_t(1) << 30) && p.N <= (int64_t(1) << 30) && p.K <= (int64_t(1) << 30);
 }
 
 template <int KIND>

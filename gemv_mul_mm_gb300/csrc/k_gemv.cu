@@ -1,35 +1,58 @@
-// k_gemv.cu -- weight-streaming quantized GEMV for small N (decode).
+// k_gemv.cu -- weight-streaming quantized GEMV for small N (decode), plain and
+// expert-grouped.
 //
-// y[n, m] = sum_k W[m, k] * x[n, k], N <= 8. Decode is bound by streaming the
-// weights from HBM once (inferencelayer 0.2.8 src/cublas_prefill.rs: "decode's
-// whole cost is streaming weights"), so the design is about bytes in flight
-// and coalescing, not arithmetic:
+// y[n, m] = sum_k W[m, k] * x[n, k] for up to 8 activation rows, and the
+// expert-indexed form where output row r reads expert expert_id[r]'s weights
+// and activation row x_row[r]. Decode is bound by streaming the weights from
+// HBM once (inferencelayer 0.2.8 src/cublas_prefill.rs: "decode's whole cost
+// is streaming weights"), so the design is about bytes in flight, coalescing
+// and a lean decode:
 //
-//   * A CTA owns groups of 32 weight rows (one row per lane) and walks them in
-//     K-chunks. One producer warp moves each chunk of the 32 rows from HBM into
-//     a shared-memory stage with 1-D bulk copies (`cp.async.bulk`, one 16-byte
-//     aligned copy per row, completing on an mbarrier, L2 evict-first); up to
-//     4 stages are in flight per SM (~100 KB), enough to cover HBM latency.
-//   * NW consumer warps split each chunk along K: warp w decodes its unit of
-//     the chunk for all 32 rows (lane = row), reading the row's bytes with
-//     16-byte shared loads (row stride padded to an odd number of 16-byte
-//     words, so the 32 lanes hit distinct banks) and the activations with
-//     broadcast loads. No cross-lane reduction; the NW partial sums per row
-//     are added through shared memory at the end of the row group.
-//   * Activations are staged once per CTA (one bulk copy when they are fp32 and
-//     16-byte aligned) in a per-format layout: for Q4_0 each block's 32 values
-//     are permuted to match the order in which two nibbles at a time are OR-ed
-//     into the mantissa of 128.0f (no int->float convert), plus one offset per
-//     block; they feed packed fp32x2 FMAs (sm_100 FFMA2), and the scale d
-//     multiplies the block's partial sum in fp32.
-//   * Persistent grid (one or two CTAs per SM) over the row groups, launched
-//     with programmatic dependent launch: the next kernel's set-up (and, when
-//     the caller declares the weights constant, its first weight stages)
-//     overlaps the tail of the previous kernel on the stream.
+//   * Work items are groups of 32 weight rows (one row per lane) of one
+//     "problem": the plain product is one problem; the grouped product has one
+//     problem per (expert, block of up to NCMAX assignments of that expert), so
+//     every touched expert's rows stream from HBM once however many tokens
+//     chose it. Each CTA (persistent, one per SM) takes a contiguous, equal
+//     share of the items.
+//   * One producer thread moves K-chunks of an item's 32 rows from HBM into a
+//     ring of shared-memory stages, one TMA tensor copy per stage
+//     (`cp.async.bulk.tensor.3d`, completing on an mbarrier, L2 evict-first).
+//     The tensor map sees the weights as (8-byte word of the row, row,
+//     expert); the box takes an odd number of 16-byte granules per row (the
+//     chunk, plus one slack granule when the chunk's count is even), so staged
+//     rows sit an odd number of 16-byte words apart and the 32 lanes reading
+//     32 rows hit distinct banks, while each box row is one contiguous run in
+//     memory (a 16-byte innermost box dimension would cost one L2 request per
+//     16 bytes). Rows past M and words past the row end read as zeros. One
+//     copy per stage (not one per row) keeps the copy engine's per-request
+//     cost off the critical path, so stages can be small and consumption
+//     starts as soon as the first one lands.
+//   * The consumer warps form G groups of NWU warps; group g consumes chunks
+//     g, g + G, g + 2G, ... of the CTA's chunk stream, warp u of the group the
+//     u-th unit of each (lane = row, 16-byte shared loads, row stride padded to
+//     an odd number of 16-byte words so the 32 lanes hit distinct banks;
+//     activations by broadcast loads). Per-row partial sums of all warps are
+//     added through shared memory at the end of each item.
+//   * Activations are staged once per problem, by the consumers, in a
+//     per-format layout. Q4_0: each nibble is OR-ed into the mantissa of
+//     128.0f at the bit position it already has in its 32-bit word (no shifts
+//     but one per word), which gives exactly 128 + q * 2^p; one packed subtract
+//     leaves exactly (q - 8) * 2^p, and the activation is staged pre-multiplied
+//     by 2^-p, so every product is the exact (q - 8) * x. Q8_0: the code byte
+//     XOR 0x80 in the low byte under 2^23 gives 2^23 + q + 128 exactly, one
+//     packed subtract leaves q. Both multiply with packed fp32x2 FMAs; the fp32
+//     block scale multiplies the block's partial sum.
+//   * Programmatic dependent launch: the kernel lets the next one on the stream
+//     launch at once, and its shared memory is small enough for two CTAs per
+//     SM, so (when the caller declares the weights constant) the next GEMV
+//     streams its first weight stages while this one drains. Activations and
+//     expert ids are read only after `griddepcontrol.wait`.
 //
-// The P4 page's v3 lesson (stage x in shared, keep lanes on distinct banks,
-// keep loads in flight) is kept; its f16x2 accumulation is not (too lossy for
-// the 1e-3 relative bar over K = 4096), nor its structure-of-arrays layout.
+// The P4 page's v3 lesson (stage x in shared memory, keep lanes on distinct
+// banks, keep loads in flight) is kept; its f16x2 accumulation is not (too
+// lossy for the 1e-3 relative bar over K = 4096), nor its structure-of-arrays
+// layout. Every wait is bounded; a timeout latches DEV_ERR_TIMEOUT and the
+// CTA unwinds.
 #include <cstdlib>
 
 #include <cuda_fp16.h>
@@ -42,38 +65,34 @@ namespace qmm {
 namespace {
 
 constexpr int kRows = 32;
-constexpr int kMaxStages = 6;
-constexpr int kSmemBudget = 220 * 1024;
+constexpr int kMaxStages = 16;
+constexpr int kCoresident = 112 * 1024;   // two CTAs (this kernel and the next) fit on one SM
+constexpr int kSmemBudget = 224 * 1024;
+constexpr int kMaxGroupedExperts = 1024;
+constexpr int kMaxGroupedAssign = 4096;
 
-// Per format: blocks per warp unit (UB) and consumer warps (NW). A unit's bytes
-// times NW (one chunk row) is a multiple of 16 for every format. Measured on
-// the decode workload (M = 14336, K = 4096): Q8_0 runs best with one CTA of 8
-// consumer warps per SM (half a row per stage), Q4_0 with 16 consumer warps
-// (a whole row per stage) -- the extra warps hide its decode latency.
+// Per format: blocks per warp unit (UB), consumer warps (NW) and preferred
+// warps per chunk (NWU). A unit is a multiple of 16 bytes where the format
+// allows it. Measured on the decode workload (M = 14336, K = 4096): Q8_0 runs
+// best with 1088-byte chunks (4 warps of 8), Q4_0 with 1152-byte chunks (8
+// warps of 16; its decode needs the extra warps).
 template <int KIND> struct SG;
-template <> struct SG<Q8_0>   { static constexpr int UB = 8,  NW = 8; };
-template <> struct SG<Q4_0>   { static constexpr int UB = 8,  NW = 16; };
-template <> struct SG<Q5_0>   { static constexpr int UB = 8,  NW = 8; };
-template <> struct SG<IQ4_NL> { static constexpr int UB = 8,  NW = 8; };
-template <> struct SG<MXFP4>  { static constexpr int UB = 16, NW = 4; };
-template <> struct SG<Q4_K>   { static constexpr int UB = 1,  NW = 8; };
-template <> struct SG<Q5_K>   { static constexpr int UB = 1,  NW = 8; };
-template <> struct SG<Q6_K>   { static constexpr int UB = 1,  NW = 8; };
-template <> struct SG<Q2_K>   { static constexpr int UB = 1,  NW = 8; };
-template <> struct SG<Q3_K>   { static constexpr int UB = 1,  NW = 8; };
-template <> struct SG<IQ4_XS> { static constexpr int UB = 1,  NW = 8; };
+template <> struct SG<Q8_0>   { static constexpr int UB = 8,  NW = 8,  NWU = 4; };
+template <> struct SG<Q4_0>   { static constexpr int UB = 8,  NW = 16, NWU = 8; };
+template <> struct SG<Q5_0>   { static constexpr int UB = 8,  NW = 8,  NWU = 2; };
+template <> struct SG<IQ4_NL> { static constexpr int UB = 8,  NW = 8,  NWU = 2; };
+template <> struct SG<MXFP4>  { static constexpr int UB = 16, NW = 8,  NWU = 2; };
+template <> struct SG<Q4_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
+template <> struct SG<Q5_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
+template <> struct SG<Q6_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
+template <> struct SG<Q2_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
+template <> struct SG<Q3_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
+template <> struct SG<IQ4_XS> { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
 
 template <int KIND> struct SGeo {
     static constexpr int NW = SG<KIND>::NW;
     static constexpr int UNIT_B = SG<KIND>::UB * Geo<KIND>::BB;
     static constexpr int UNIT_E = SG<KIND>::UB * Geo<KIND>::BE;
-    static constexpr int CHUNK_B = NW * UNIT_B;
-    static constexpr int CHUNK_E = NW * UNIT_E;
-    static constexpr int STRIDE = CHUNK_B + (((CHUNK_B / 16) % 2 == 0) ? 16 : 32);
-    static constexpr int STAGE_B = kRows * STRIDE;
-    static constexpr bool PARTIAL_OK = (UNIT_B % 16) == 0;  // a partial chunk is whole 16-byte rows
-    static_assert(CHUNK_B % 16 == 0, "a chunk row must be whole 16-byte vectors");
-    static_assert(STRIDE % 16 == 0 && (STRIDE / 16) % 2 == 1, "padded row stride");
 };
 
 struct GemvArgs {
@@ -83,32 +102,55 @@ struct GemvArgs {
     int K;
     const void* X;
     int x_dtype;
-    int ncols;      // valid columns (<= NCOL)
     float* Y;
+    int ncols;                // plain: N
+    // grouped (x_row == nullptr for the plain product)
+    const int32_t* x_row;
+    const int32_t* expert_id;
+    size_t expert_stride;
+    int n_experts;
+    int n_assign;
+    int64_t n_x_rows;
+    // pipeline
     int stages;
-    int flags;      // kFlagPrefetchW | kFlagBulkX
+    int nwu;                  // warps per chunk
+    int stride;               // shared bytes per staged row: box granules * 16 (odd multiple of 16)
+    int upr;                  // units per row
+    int cpr;                  // chunks per row
+    int flags;
     unsigned* err;
 };
 
 constexpr int kFlagPrefetchW = 1;  // weights may be read before the previous grid completes
-constexpr int kFlagBulkX = 2;      // activations are fp32, 16-byte aligned: one bulk copy
-
-__device__ __forceinline__ float load_x(const void* X, int xdt, int64_t i) {
-    if (xdt == 1) return __half2float(reinterpret_cast<const __half*>(X)[i]);
-    return reinterpret_cast<const float*>(X)[i];
-}
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 3-D tiled TMA load (coordinates innermost first), completing on `bar`, with
+// an L2 cache policy.
+__device__ __forceinline__ void tma3d(void* dst, const CUtensorMap* tm, int c0, int c1, int c2, uint64_t* bar,
+                                      uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// (a & b) | c in one LOP3, all operands in registers.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 // ---------------------------------------------------------------------------
 // unit decoders: acc[n] += sum over the unit's elements of W * x[n]
 // ---------------------------------------------------------------------------
 
 // Any format, from shared bytes (scale applied per element).
-template <int KIND, int NCOL>
-__device__ __forceinline__ void unit_generic(const uint8_t* u, const float* xs, const float*, int K, int k0,
-                                             float (&acc)[NCOL]) {
+template <int KIND, int NC>
+__device__ __forceinline__ void unit_generic(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
     constexpr int BB = Geo<KIND>::BB, BE = Geo<KIND>::BE, UB = SG<KIND>::UB;
 #pragma unroll 1
     for (int blk = 0; blk < UB; ++blk) {
@@ -116,35 +158,26 @@ __device__ __forceinline__ void unit_generic(const uint8_t* u, const float* xs, 
 #pragma unroll 1
         for (int j = 0; j < BE / 32; ++j) {
             const int kb = k0 + blk * BE + 32 * j;
-            float s[NCOL];
+            float s[NC];
 #pragma unroll
-            for (int n = 0; n < NCOL; ++n) s[n] = 0.f;
+            for (int n = 0; n < NC; ++n) s[n] = 0.f;
 #pragma unroll 8
             for (int i = 0; i < 32; ++i) {
                 const float v = elem32<KIND>(b, j, i);
 #pragma unroll
-                for (int n = 0; n < NCOL; ++n) s[n] = fmaf(v, xs[n * K + kb + i], s[n]);
+                for (int n = 0; n < NC; ++n) s[n] = fmaf(v, xs[n * K + kb + i], s[n]);
             }
 #pragma unroll
-            for (int n = 0; n < NCOL; ++n) acc[n] += s[n];
+            for (int n = 0; n < NC; ++n) acc[n] += s[n];
         }
     }
 }
 
-// (a & b) | c in one LOP3 with all three operands in registers (an immediate
-// mask plus an immediate constant would otherwise take two instructions).
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
-// Q4_0 staged-activation order. Within a block the decoder walks four 32-bit
-// words of code bytes; a word holding code bytes (b0, b1, b2, b3) yields the
-// low nibbles of (b0, b2), then of (b1, b3), then the high nibbles of (b0, b2)
-// and of (b1, b3). Odd blocks start 4-byte aligned (word j = bytes 4j..4j+3);
-// even blocks start 2 bytes off, so their words are [14, 15, 0, 1] and then
-// bytes 4j-2..4j+1. q4_slot(e, even) is the staged position of element e.
+// Q4_0 staged-activation order. The decoder walks four 32-bit words of code
+// bytes per block. Odd blocks start 4-byte aligned at their codes (word j =
+// code bytes 4j..4j+3); even blocks start 2 bytes off, so their word 0 is
+// (c14, c15, c0, c1) and word j >= 1 holds code bytes 4j-2..4j+1. Nibble i of a
+// word (bits 4i..4i+3; i = 2 * byte + high) feeds slot 8j + i.
 __host__ __device__ __forceinline__ int q4_slot(int e, bool even) {
     const int hi = e >> 4, c = e & 15;       // nibble half, code byte
     int j, k;                                // word, byte within word
@@ -161,19 +194,20 @@ __host__ __device__ __forceinline__ int q4_slot(int e, bool even) {
         j = (c + 2) >> 2;
         k = (c + 2) & 3;
     }
-    // word j's 8 slots: lo (b0, b2, b1, b3), then hi (b0, b2, b1, b3)
-    const int within = (k & 1) * 2 + (k >> 1);
-    return 8 * j + 4 * hi + within;
+    return 8 * j + 2 * k + hi;
+}
+
+// Nibble i of a word is OR-ed into 128.0f at mantissa bits 4i..4i+3 (i <= 4)
+// or, from the word shifted right by 12, at bits 4(i-3)..4(i-3)+3 (i >= 5):
+// its weight there is 2^(4i-16) resp. 2^(4(i-3)-16). The activation staged for
+// that slot is multiplied by the inverse power of two (exact).
+__host__ __device__ __forceinline__ int q4_pow(int i) {
+    return (i <= 4) ? 4 * i - 16 : 4 * (i - 3) - 16;
 }
 
 // Q4_0: 8 blocks of 18 bytes (144 B, 16-byte aligned in shared memory).
-// One LOP3 turns the low nibbles of bytes 0 and 2 of a word into 0x430q_000p:
-// read as fp32 it is 128 + q (+ p / 65536, far below the 1e-3 bar), and one
-// IMAD (x 65536 + 0x43000000, on the FMA pipe) turns its low half into exactly
-// 128 + p. So S = sum (128 + q) x and sum (q - 8) x = S - 136 * sum x = S - cb.
-template <int NCOL>
-__device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, const float* cb, int K, int k0,
-                                          float (&acc)[NCOL]) {
+template <int NC>
+__device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
     uint32_t w[36];
 #pragma unroll
     for (int i = 0; i < 9; ++i) {
@@ -183,8 +217,13 @@ __device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, con
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
     }
-    const int nb32 = K / 32;
-    const uint32_t kMask = 0x000F000Fu, kMagic = 0x43000000u;
+    const uint32_t mask[5] = {0xFu, 0xF0u, 0xF00u, 0xF000u, 0xF0000u};
+    const uint32_t kMagic = 0x43000000u;   // 128.0f
+    // 128 + 8 * 2^p for the four nibble pairs (0,1) (2,3) (4,5) (6,7)
+    const float2 bias0 = make_float2(128.f + 8.f * 0x1p-16f, 128.f + 8.f * 0x1p-12f);
+    const float2 bias1 = make_float2(128.f + 8.f * 0x1p-8f, 128.f + 8.f * 0x1p-4f);
+    const float2 bias2 = make_float2(136.f, 128.f + 8.f * 0x1p-8f);
+    const float2 bias3 = make_float2(128.f + 8.f * 0x1p-4f, 136.f);
 #pragma unroll
     for (int blk = 0; blk < 8; ++blk) {
         const int o = 18 * blk, a = o >> 2;
@@ -203,34 +242,38 @@ __device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, con
             words[3] = w[a + 4];
         }
         const int kb = k0 + 32 * blk;
-        float2 S[NCOL][2];
+        float2 S[NC][2];
 #pragma unroll
-        for (int n = 0; n < NCOL; ++n) S[n][0] = S[n][1] = make_float2(0.f, 0.f);
+        for (int n = 0; n < NC; ++n) S[n][0] = S[n][1] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t v = words[j];
-            const uint32_t t0 = and_or(v, kMask, kMagic);
-            const uint32_t t1 = and_or(v >> 8, kMask, kMagic);
-            const uint32_t t2 = and_or(v >> 4, kMask, kMagic);
-            const uint32_t t3 = and_or(v >> 12, kMask, kMagic);
-            const float2 f0 = make_float2(__uint_as_float(t0 * 65536u + kMagic), __uint_as_float(t0));
-            const float2 f1 = make_float2(__uint_as_float(t1 * 65536u + kMagic), __uint_as_float(t1));
-            const float2 f2 = make_float2(__uint_as_float(t2 * 65536u + kMagic), __uint_as_float(t2));
-            const float2 f3 = make_float2(__uint_as_float(t3 * 65536u + kMagic), __uint_as_float(t3));
+            const uint32_t v = words[j], sh = v >> 12;
+            const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[0], kMagic)),
+                                                      __uint_as_float(and_or(v, mask[1], kMagic))),
+                                          make_float2(-bias0.x, -bias0.y));
+            const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[2], kMagic)),
+                                                      __uint_as_float(and_or(v, mask[3], kMagic))),
+                                          make_float2(-bias1.x, -bias1.y));
+            const float2 f45 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[4], kMagic)),
+                                                      __uint_as_float(and_or(sh, mask[2], kMagic))),
+                                          make_float2(-bias2.x, -bias2.y));
+            const float2 f67 = __fadd2_rn(make_float2(__uint_as_float(and_or(sh, mask[3], kMagic)),
+                                                      __uint_as_float(and_or(sh, mask[4], kMagic))),
+                                          make_float2(-bias3.x, -bias3.y));
 #pragma unroll
-            for (int n = 0; n < NCOL; ++n) {
+            for (int n = 0; n < NC; ++n) {
                 const float4 xl = *reinterpret_cast<const float4*>(xs + n * K + kb + 8 * j);
                 const float4 xh = *reinterpret_cast<const float4*>(xs + n * K + kb + 8 * j + 4);
-                S[n][0] = __ffma2_rn(f0, make_float2(xl.x, xl.y), S[n][0]);
-                S[n][1] = __ffma2_rn(f1, make_float2(xl.z, xl.w), S[n][1]);
-                S[n][0] = __ffma2_rn(f2, make_float2(xh.x, xh.y), S[n][0]);
-                S[n][1] = __ffma2_rn(f3, make_float2(xh.z, xh.w), S[n][1]);
+                S[n][0] = __ffma2_rn(f01, make_float2(xl.x, xl.y), S[n][0]);
+                S[n][1] = __ffma2_rn(f23, make_float2(xl.z, xl.w), S[n][1]);
+                S[n][0] = __ffma2_rn(f45, make_float2(xh.x, xh.y), S[n][0]);
+                S[n][1] = __ffma2_rn(f67, make_float2(xh.z, xh.w), S[n][1]);
             }
         }
 #pragma unroll
-        for (int n = 0; n < NCOL; ++n) {
+        for (int n = 0; n < NC; ++n) {
             const float2 t2 = __fadd2_rn(S[n][0], S[n][1]);
-            acc[n] = fmaf(d, (t2.x + t2.y) - cb[n * nb32 + (kb >> 5)], acc[n]);
+            acc[n] = fmaf(d, t2.x + t2.y, acc[n]);
         }
     }
 }
@@ -238,9 +281,8 @@ __device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, con
 // Q8_0: 8 blocks of 34 bytes (272 B). Code byte c (two's complement) XOR 0x80
 // is c + 128; placed in the low byte under 0x4B000000 it reads 2^23 + c + 128,
 // and one packed subtract of (2^23 + 128) leaves c exactly.
-template <int NCOL>
-__device__ __forceinline__ void unit_q8_0(const uint8_t* u, const float* xs, const float*, int K, int k0,
-                                          float (&acc)[NCOL]) {
+template <int NC>
+__device__ __forceinline__ void unit_q8_0(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
     uint32_t w[68];
 #pragma unroll
     for (int i = 0; i < 17; ++i) {
@@ -257,14 +299,14 @@ __device__ __forceinline__ void unit_q8_0(const uint8_t* u, const float* xs, con
         const uint32_t dw = w[o >> 2];
         const float d = h2f((o & 3) ? (dw >> 16) : dw);
         const int kb = k0 + 32 * blk;
-        float2 S[NCOL][2];
+        float2 S[NC][2];
 #pragma unroll
-        for (int n = 0; n < NCOL; ++n) S[n][0] = S[n][1] = make_float2(0.f, 0.f);
+        for (int n = 0; n < NC; ++n) S[n][0] = S[n][1] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-            float4 xv[NCOL];
+            float4 xv[NC];
 #pragma unroll
-            for (int n = 0; n < NCOL; ++n) xv[n] = *reinterpret_cast<const float4*>(xs + n * K + kb + i);
+            for (int n = 0; n < NC; ++n) xv[n] = *reinterpret_cast<const float4*>(xs + n * K + kb + i);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int b0 = o + 2 + i + 2 * h, b1 = b0 + 1;
@@ -274,218 +316,400 @@ __device__ __forceinline__ void unit_q8_0(const uint8_t* u, const float* xs, con
                     __byte_perm(w[b1 >> 2] ^ 0x80808080u, 0x4B000000u, 0x7650u | static_cast<unsigned>(b1 & 3))));
                 const float2 q = __fadd2_rn(make_float2(f0, f1), off);
 #pragma unroll
-                for (int n = 0; n < NCOL; ++n) {
+                for (int n = 0; n < NC; ++n) {
                     const float2 xp = h ? make_float2(xv[n].z, xv[n].w) : make_float2(xv[n].x, xv[n].y);
                     S[n][h] = __ffma2_rn(q, xp, S[n][h]);
                 }
             }
         }
 #pragma unroll
-        for (int n = 0; n < NCOL; ++n) {
+        for (int n = 0; n < NC; ++n) {
             const float2 t2 = __fadd2_rn(S[n][0], S[n][1]);
             acc[n] = fmaf(d, t2.x + t2.y, acc[n]);
         }
     }
 }
 
-template <int KIND, int NCOL>
-__device__ __forceinline__ void unit(const uint8_t* u, const float* xs, const float* cb, int K, int k0,
-                                     float (&acc)[NCOL]) {
-    // the Q4_0 / Q8_0 decoders take eight blocks (a 16-byte multiple) at a time
-    if constexpr (KIND == Q4_0 || KIND == Q8_0) {
-        static_assert(SG<KIND>::UB % 8 == 0, "Q4_0 / Q8_0 units are whole groups of eight blocks");
-#pragma unroll
-        for (int h = 0; h < SG<KIND>::UB / 8; ++h) {
-            if constexpr (KIND == Q4_0) unit_q4_0<NCOL>(u + h * 8 * 18, xs, cb, K, k0 + h * 256, acc);
-            else unit_q8_0<NCOL>(u + h * 8 * 34, xs, cb, K, k0 + h * 256, acc);
-        }
-    } else {
-        unit_generic<KIND, NCOL>(u, xs, cb, K, k0, acc);
-    }
-}
-
-template <int KIND> __host__ __device__ constexpr int cb_floats(int K, int ncol) { return KIND == Q4_0 ? ncol * (K / 32) : 0; }
-// Q4_0 stages the raw activations apart from the permuted copy.
-template <int KIND> __host__ __device__ constexpr int raw_floats(int K, int ncol) { return KIND == Q4_0 ? ncol * K : 0; }
-
-// Activation staging by the consumer threads, after the raw fp32 activations
-// are in `raw` (bulk copy; nullptr = read them from global memory). Q4_0
-// permutes each block into decode order (a permutation within 32 words, so a
-// warp's stores hit 32 distinct banks) and stores 136 * (sum of the block) in
-// cb, one block per thread with a lane-rotated walk (conflict-free); the other
-// formats keep the natural order.
-template <int KIND, int NCOL>
-__device__ void stage_x(const GemvArgs& a, float* xs, float* cb, const float* raw, int tid, int nthr) {
-    const int K = a.K;
-    auto xval = [&](int n, int k) -> float {
-        if (n >= a.ncols) return 0.f;
-        return raw ? raw[n * K + k] : load_x(a.X, a.x_dtype, static_cast<int64_t>(n) * K + k);
-    };
+template <int KIND, int NC>
+__device__ __forceinline__ void unit(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
     if constexpr (KIND == Q4_0) {
-        for (int n = 0; n < NCOL; ++n)
-            for (int k = tid; k < K; k += nthr) {
-                const int b = k >> 5, e = k & 31;
-                xs[n * K + 32 * b + q4_slot(e, (b & 1) == 0)] = xval(n, k);
-            }
-        const int nb = K / 32;
-        for (int i = tid; i < NCOL * nb; i += nthr) {
-            const int n = i / nb, b = i - n * nb;
-            float sum = 0.f;
-            for (int e = 0; e < 32; ++e) sum += xval(n, 32 * b + ((e + tid) & 31));
-            cb[i] = 136.f * sum;
-        }
+        static_assert(SG<KIND>::UB == 8, "the Q4_0 decoder takes eight blocks");
+        unit_q4_0<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == Q8_0) {
+        static_assert(SG<KIND>::UB == 8, "the Q8_0 decoder takes eight blocks");
+        unit_q8_0<NC>(u, xs, K, k0, acc);
     } else {
-        for (int n = 0; n < NCOL; ++n)
-            for (int k = tid; k < K; k += nthr) {
-                if (raw && n < a.ncols) continue;   // already in place
-                xs[n * K + k] = xval(n, k);
-            }
+        unit_generic<KIND, NC>(u, xs, K, k0, acc);
     }
 }
 
-// Shared-memory layout of one CTA.
-template <int KIND, int NCOL>
-struct Smem {
-    uint8_t* stage0;
-    float* xs;
-    float* cb;
-    float* raw;        // bulk-copy target of the activations
-    float* red;        // [2][NCOL][NW][32]
-    uint64_t* full;    // [kMaxStages]
-    uint64_t* empty;   // [kMaxStages]
-    uint64_t* red_full;   // [2]
-    uint64_t* red_empty;  // [2]
-    uint64_t* x_full;
-    int* abort_flag;
+// ---------------------------------------------------------------------------
+// shared-memory layout
+// ---------------------------------------------------------------------------
+struct Lay {
+    int xs, red, tbl, bars, total;
+};
 
-    __host__ __device__ static size_t bytes(int K, int stages) {
-        using G = SGeo<KIND>;
-        size_t b = static_cast<size_t>(stages) * G::STAGE_B;
-        b += sizeof(float) * (static_cast<size_t>(NCOL) * K + cb_floats<KIND>(K, NCOL) + raw_floats<KIND>(K, NCOL) +
-                              2 * NCOL * G::NW * 32);
-        b = (b + 7) & ~size_t(7);
-        b += (2 * kMaxStages + 5) * sizeof(uint64_t) + 16;
-        return b;
-    }
+// Grouped tables (int32): ecnt[E + 1] (last = bad ids), eoff[E + 2],
+// ioff[E + 2] (items before expert e), pos[A], order[A], misc[4].
+__host__ __device__ __forceinline__ int tbl_ints(int E, int A) { return 3 * (E + 2) + 2 * A + 4; }
 
-    __device__ Smem(uint8_t* base, int K, int stages) {
-        using G = SGeo<KIND>;
-        stage0 = base;
-        xs = reinterpret_cast<float*>(base + stages * G::STAGE_B);
-        cb = xs + NCOL * K;
-        raw = raw_floats<KIND>(K, NCOL) ? cb + cb_floats<KIND>(K, NCOL) : xs;
-        red = cb + cb_floats<KIND>(K, NCOL) + raw_floats<KIND>(K, NCOL);
-        full = reinterpret_cast<uint64_t*>(
-            (reinterpret_cast<uintptr_t>(red + 2 * NCOL * G::NW * 32) + 7) & ~static_cast<uintptr_t>(7));
-        empty = full + kMaxStages;
-        red_full = empty + kMaxStages;
-        red_empty = red_full + 2;
-        x_full = red_empty + 2;
-        abort_flag = reinterpret_cast<int*>(x_full + 1);
+__host__ __device__ __forceinline__ Lay layout(int stage_b, int stages, int ncmax, int K, int nw, bool grouped, int E,
+                                               int A) {
+    Lay l;
+    int off = stages * stage_b;
+    l.xs = off;
+    off += ncmax * K * 4;
+    l.red = off;
+    off += 2 * ncmax * nw * 32 * 4;
+    l.tbl = off;
+    off += grouped ? tbl_ints(E, A) * 4 : 0;
+    off = (off + 15) & ~15;
+    l.bars = off;
+    off += (2 * kMaxStages + 6) * 8 + 16;
+    l.total = off + 128;   // + slack to align the base to 128 bytes
+    return l;
+}
+
+struct Tables {
+    int* ecnt;
+    int* eoff;
+    int* ioff;
+    int* pos;
+    int* order;
+    int* misc;   // [0] total items, [1] bad count
+};
+
+__device__ __forceinline__ Tables tables(uint8_t* base, int E, int A) {
+    Tables t;
+    int* p = reinterpret_cast<int*>(base);
+    t.ecnt = p;
+    t.eoff = p + (E + 2);
+    t.ioff = p + 2 * (E + 2);
+    t.pos = p + 3 * (E + 2);
+    t.order = t.pos + A;
+    t.misc = t.order + A;
+    return t;
+}
+
+// One work item: 32 rows (row group g) of expert e, columns [col0, col0 + ncol).
+struct Item {
+    int e, col0, ncol;
+    int64_t g;
+};
+
+// Walks the CTA's contiguous item range in order (plain: one problem).
+struct ItemWalker {
+    int e = 0;
+    __device__ __forceinline__ Item at(int64_t i, const GemvArgs& a, const Tables& t, int64_t rg, int ncmax) {
+        Item it;
+        if (!a.x_row) {
+            it.e = 0;
+            it.col0 = 0;
+            it.ncol = a.ncols;
+            it.g = i;
+            return it;
+        }
+        while (t.ioff[e + 1] <= i) ++e;
+        const int64_t local = i - t.ioff[e];
+        const int b = static_cast<int>(local / rg);
+        it.e = e;
+        it.g = local - static_cast<int64_t>(b) * rg;
+        it.col0 = t.eoff[e] + b * ncmax;
+        it.ncol = min(ncmax, t.ecnt[e] - b * ncmax);
+        return it;
     }
 };
 
-template <int KIND, int NCOL>
-__global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32) k_gemv(GemvArgs a) {
+// Bucket the assignments by expert, in assignment order (deterministic: every
+// CTA builds the same tables). Run by one warp after the CTA has written each
+// assignment's bucket (expert id, or E for a bad id or activation row) to
+// pos[]. On return pos[r] = bucket << 16 | rank of r within its bucket.
+__device__ void build_tables(const GemvArgs& a, const Tables& t, int64_t rg, int ncmax, int lane) {
+    const unsigned full = 0xffffffffu;
+    const int E = a.n_experts, A = a.n_assign;
+    for (int e = lane; e <= E; e += 32) t.ecnt[e] = 0;
+    __syncwarp();
+    for (int r0 = 0; r0 < A; r0 += 32) {
+        const int r = r0 + lane;
+        const bool act = r < A;
+        const int key = act ? t.pos[r] : -1;
+        const unsigned same = __match_any_sync(full, key);
+        const int rank = __popc(same & ((1u << lane) - 1u));
+        const int base = act ? t.ecnt[key] : 0;
+        __syncwarp();
+        if (act) {
+            t.pos[r] = (key << 16) | (base + rank);
+            if (rank == 0) t.ecnt[key] = base + __popc(same);
+        }
+        __syncwarp();
+    }
+    // exclusive scans over buckets 0..E of the assignment counts and of the
+    // work items (row groups x column blocks), one run of buckets per lane
+    const int per = (E + 1 + 31) / 32;
+    const int e0 = min(E + 1, lane * per), e1 = min(E + 1, e0 + per);
+    const int rgi = static_cast<int>(rg);
+    int cs = 0, is = 0;
+    for (int e = e0; e < e1; ++e) {
+        cs += t.ecnt[e];
+        if (e < E) is += ((t.ecnt[e] + ncmax - 1) / ncmax) * rgi;
+    }
+    int ci = cs, ii = is;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int c2 = __shfl_up_sync(full, ci, off), i2 = __shfl_up_sync(full, ii, off);
+        if (lane >= off) {
+            ci += c2;
+            ii += i2;
+        }
+    }
+    const int ctot = __shfl_sync(full, ci, 31), itot = __shfl_sync(full, ii, 31);
+    int cx = ci - cs, ix = ii - is;
+    for (int e = e0; e < e1; ++e) {
+        t.eoff[e] = cx;
+        t.ioff[e] = ix;
+        cx += t.ecnt[e];
+        if (e < E) ix += ((t.ecnt[e] + ncmax - 1) / ncmax) * rgi;
+    }
+    __syncwarp();
+    if (lane == 0) {
+        t.eoff[E + 1] = ctot;
+        t.ioff[E + 1] = itot;
+        t.misc[0] = itot;
+        t.misc[1] = t.ecnt[E];
+    }
+    __syncwarp();
+    for (int r = lane; r < A; r += 32) {
+        const int v = t.pos[r];
+        t.order[t.eoff[v >> 16] + (v & 0xFFFF)] = r;
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ float load_x(const void* X, int xdt, int64_t i) {
+    if (xdt == 1) return __half2float(reinterpret_cast<const __half*>(X)[i]);
+    return reinterpret_cast<const float*>(X)[i];
+}
+
+// Stage the activations of columns [col0, col0 + ncol) (zeros up to NCMAX) in
+// the format's layout. Consumers only. Each thread issues a batch of eight
+// 16-byte loads before it stores any of them, so the staging costs one L2
+// round trip per batch instead of one per load.
+template <int KIND, int NCMAX>
+__device__ void stage_x(const GemvArgs& a, const Tables& t, const Item& it, float* xs, int tid, int nthr) {
+    constexpr int B = 8;
+    const int K = a.K;
+    const int kq = K / 4;
+    const int total = NCMAX * kq;
+    const bool vec = a.x_dtype == 0 && (reinterpret_cast<uintptr_t>(a.X) & 15) == 0;
+    for (int base = tid; base < total; base += B * nthr) {
+        float4 v[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int idx = base + j * nthr;
+            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (idx < total) {
+                const int n = idx / kq, k = 4 * (idx - n * kq);
+                if (n < it.ncol) {
+                    const int64_t row = a.x_row ? static_cast<int64_t>(a.x_row[t.order[it.col0 + n]]) : n;
+                    const int64_t off = row * K + k;
+                    if (vec) {
+                        v[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.X) + off);
+                    } else {
+                        v[j].x = load_x(a.X, a.x_dtype, off);
+                        v[j].y = load_x(a.X, a.x_dtype, off + 1);
+                        v[j].z = load_x(a.X, a.x_dtype, off + 2);
+                        v[j].w = load_x(a.X, a.x_dtype, off + 3);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int idx = base + j * nthr;
+            if (idx >= total) break;
+            const int n = idx / kq, k = 4 * (idx - n * kq);
+            if constexpr (KIND == Q4_0) {
+                const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int kk = k + c, b = kk >> 5, e = kk & 31;
+                    const int slot = q4_slot(e, (b & 1) == 0);
+                    // times 2^-p, an exact power-of-two product
+                    xs[n * K + 32 * b + slot] = vv[c] * __int_as_float((127 - q4_pow(slot & 7)) << 23);
+                }
+            } else {
+                *reinterpret_cast<float4*>(xs + n * K + k) = v[j];
+            }
+        }
+    }
+}
+
+template <int KIND, int NC, int NCMAX>
+__device__ __forceinline__ void consume_item(const GemvArgs& a, const Tables& t, const Item& item, uint8_t* stage0,
+                                             int stage_b, const float* xs, float* red, uint64_t* full,
+                                             uint64_t* empty, uint64_t* red_full, uint64_t* red_empty,
+                                             volatile int* abort_flag, int it_base, int gi, int warp, int lane) {
     using G = SGeo<KIND>;
     constexpr int NW = G::NW;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int K = a.K;
-    Smem<KIND, NCOL> sm(smem, K, a.stages);
-    volatile int* abort_flag = sm.abort_flag;
+    const int nwu = a.nwu, ngroups = NW / nwu, grp = warp / nwu, u = warp - grp * nwu;
+    const int S = a.stages, K = a.K;
+    float acc[NC];
+#pragma unroll
+    for (int n = 0; n < NC; ++n) acc[n] = 0.f;
+    // first chunk of this item handled by my group
+    int c = (grp - it_base % ngroups + ngroups) % ngroups;
+    for (; c < a.cpr; c += ngroups) {
+        const int it = it_base + c;
+        const int s = it % S, use = it / S;
+        const bool ok = !*abort_flag && mbar_wait(&full[s], use & 1, abort_flag, a.err);
+        const int units = min(nwu, a.upr - c * nwu);
+        if (ok && u < units)
+            unit<KIND, NC>(stage0 + s * stage_b + lane * a.stride + u * G::UNIT_B, xs, K,
+                           (c * nwu + u) * G::UNIT_E, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // cross-warp sum through shared memory; the item's writer warp (rotating)
+    // waits, adds and stores
+    const int p = gi & 1, use = gi >> 1;
+    float* rb = red + p * NCMAX * NW * 32;   // fixed stride: items may differ in NC
+    if (use > 0 && !*abort_flag) mbar_wait(&red_empty[p], (use - 1) & 1, abort_flag, a.err);
+#pragma unroll
+    for (int n = 0; n < NC; ++n) rb[(n * NW + warp) * 32 + lane] = acc[n];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&red_full[p]);
+    if (warp == gi % NW) {
+        const bool ok = !*abort_flag && mbar_wait(&red_full[p], use & 1, abort_flag, a.err);
+        const int64_t row = item.g * kRows + lane;
+        if (ok && row < a.M) {
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                if (n < item.ncol) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) v += rb[(n * NW + w) * 32 + lane];
+                    const int64_t r = a.x_row ? static_cast<int64_t>(t.order[item.col0 + n]) : n;
+                    a.Y[r * a.M + row] = v;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&red_empty[p]);
+    }
+}
 
-    // Let the next kernel on the stream start its set-up as our CTAs retire.
+// Q4_0 (17 warps) gets the registers of one CTA per SM: its decoder spills at
+// the 60 registers two such CTAs would allow. The other formats keep room for
+// a second CTA (the next kernel's, under programmatic dependent launch).
+template <int KIND> struct MinBlocks { static constexpr int V = (KIND == Q4_0) ? 1 : 2; };
+
+template <int KIND, int NCMAX>
+__global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32, MinBlocks<KIND>::V)
+    k_gemv(const __grid_constant__ CUtensorMap tmW, GemvArgs a) {
+    using G = SGeo<KIND>;
+    constexpr int NW = G::NW;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // 128-byte aligned base (TMA tensor destinations), by arithmetic on the
+    // shared array so that accesses stay shared-memory loads and stores
+    uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    const bool grouped = a.x_row != nullptr;
+    const int K = a.K;
+    const int stage_b = kRows * a.stride;
+    const Lay L = layout(stage_b, a.stages, NCMAX, K, NW, grouped, a.n_experts, a.n_assign);
+    uint8_t* stage0 = smem;
+    float* xs = reinterpret_cast<float*>(smem + L.xs);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    const Tables T = tables(smem + L.tbl, a.n_experts, a.n_assign);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* red_full = empty + kMaxStages;
+    uint64_t* red_empty = red_full + 2;
+    uint64_t* tbl_ready = red_empty + 2;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tbl_ready + 1);
+
+    // Let the next kernel on the stream start its set-up as soon as possible.
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], NW);
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], a.nwu);
         }
         for (int p = 0; p < 2; ++p) {
-            mbar_init(&sm.red_full[p], NW);
-            mbar_init(&sm.red_empty[p], 1);
+            mbar_init(&red_full[p], NW);
+            mbar_init(&red_empty[p], 1);
         }
-        mbar_init(sm.x_full, 1);
+        mbar_init(tbl_ready, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
-    const int64_t ngroups = (a.M + kRows - 1) / kRows;
-    const int nchunks = (K + G::CHUNK_E - 1) / G::CHUNK_E;
-    const int ST = a.stages;
-    const bool bulk_x = (a.flags & kFlagBulkX) != 0;
+    const int64_t rg = (a.M + kRows - 1) / kRows;   // row groups per problem
+    const int S = a.stages;
+    if (grouped) {
+        // the expert ids come from earlier kernels: wait for them, then every
+        // thread files a share of the assignments into their buckets
+        grid_dep_wait();
+        for (int r = threadIdx.x; r < a.n_assign; r += blockDim.x) {
+            const int e = a.expert_id[r];
+            const int64_t xr = a.x_row[r];
+            T.pos[r] = (e >= 0 && e < a.n_experts && xr >= 0 && xr < a.n_x_rows) ? e : a.n_experts;
+        }
+        __syncthreads();
+    }
 
     if (warp == NW) {
         // ---------------- producer warp ----------------
         const uint64_t pol = l2_evict_first_policy();
-        int it = 0;
+        int64_t n_items = rg;
         bool waited = false;
-        if (!(a.flags & kFlagPrefetchW)) {
+        if (grouped || !(a.flags & kFlagPrefetchW)) {
             grid_dep_wait();
             waited = true;
         }
-        for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
-            const int rows = static_cast<int>(imin64(kRows, a.M - g * kRows));
-            const uint8_t* wg = a.W + static_cast<size_t>(g * kRows) * a.row_bytes;
-            for (int kc = 0; kc < nchunks; ++kc, ++it) {
-                const int s = it % ST, use = it / ST;
+        if (grouped) {
+            build_tables(a, T, rg, NCMAX, lane);
+            n_items = T.misc[0];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tbl_ready);
+        }
+        const int64_t lo = static_cast<int64_t>(blockIdx.x) * n_items / gridDim.x;
+        const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * n_items / gridDim.x;
+        ItemWalker walk;
+        int it = 0;
+        const uint32_t box_bytes = static_cast<uint32_t>(stage_b);
+        const int cg = a.nwu * G::UNIT_B / 16;   // granules per chunk
+        for (int64_t i = lo; i < hi; ++i) {
+            const Item item = walk.at(i, a, T, rg, NCMAX);
+            for (int c = 0; c < a.cpr; ++c, ++it) {
+                const int s = it % S, use = it / S;
                 if (use > 0 && !waited) {
-                    // all prefetched stages are issued: now the activations
+                    // every prefetch stage is issued: wait for the previous grid
                     grid_dep_wait();
                     waited = true;
-                    if (bulk_x && lane == 0) {
-                        const uint32_t xb = static_cast<uint32_t>(a.ncols) * K * 4u;
-                        mbar_arrive_expect_tx(sm.x_full, xb);
-                        bulk_g2s(sm.raw, a.X, xb, sm.x_full);
-                    }
                 }
-                if (use > 0 && !mbar_wait(&sm.empty[s], (use - 1) & 1, abort_flag, a.err)) goto drain;
-                const int units = min(NW, (K - kc * G::CHUNK_E) / G::UNIT_E);
-                const uint32_t bytes = static_cast<uint32_t>(units * G::UNIT_B);
-                if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], static_cast<uint32_t>(rows) * bytes);
+                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, abort_flag, a.err)) goto drain;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[s], box_bytes);
+                    // innermost coordinate in 8-byte words: a multiple of two (16-byte aligned)
+                    tma3d(stage0 + s * stage_b, &tmW, 2 * c * cg, static_cast<int>(item.g * kRows), item.e, &full[s],
+                          pol);
+                }
                 __syncwarp();
-                if (lane < rows)
-                    bulk_g2s_hint(sm.stage0 + s * G::STAGE_B + lane * G::STRIDE,
-                                  wg + static_cast<size_t>(lane) * a.row_bytes + static_cast<size_t>(kc) * G::CHUNK_B,
-                                  bytes, &sm.full[s], pol);
-                if (waited && it == 0 && bulk_x && lane == 0) {
-                    const uint32_t xb = static_cast<uint32_t>(a.ncols) * K * 4u;
-                    mbar_arrive_expect_tx(sm.x_full, xb);
-                    bulk_g2s(sm.raw, a.X, xb, sm.x_full);
-                }
             }
         }
-        if (!waited) {
-            // every stage fit in the prefetch window
-            grid_dep_wait();
-            waited = true;
-            if (bulk_x && lane == 0) {
-                const uint32_t xb = static_cast<uint32_t>(a.ncols) * K * 4u;
-                mbar_arrive_expect_tx(sm.x_full, xb);
-                bulk_g2s(sm.raw, a.X, xb, sm.x_full);
-            }
-        }
+        if (!waited) grid_dep_wait();
     drain:
         // Before the CTA can retire, every issued copy must have landed: wait
-        // (bounded, ignoring the abort flag) for the last phase of each stage
-        // and for the activation copy.
+        // (bounded, ignoring the abort flag) for the last phase of each stage.
         {
             const int issued = it;
-            for (int s = 0; s < ST && s < issued; ++s) {
-                const int last_use = (issued - 1 - s) / ST;  // uses of slot s: it = s + ST*use
+            for (int s = 0; s < S && s < issued; ++s) {
+                const int last_use = (issued - 1 - s) / S;   // uses of slot s: it = s + S * use
                 const long long t0 = clock64();
-                while (!mbar_try_wait(&sm.full[s], last_use & 1)) {
-                    if (clock64() - t0 > (1ll << 31)) {
-                        atomicOr(a.err, DEV_ERR_TIMEOUT);
-                        break;
-                    }
-                }
-            }
-            if (bulk_x && waited) {
-                const long long t0 = clock64();
-                while (!mbar_try_wait(sm.x_full, 0)) {
+                while (!mbar_try_wait(&full[s], last_use & 1)) {
                     if (clock64() - t0 > (1ll << 31)) {
                         atomicOr(a.err, DEV_ERR_TIMEOUT);
                         break;
@@ -498,135 +722,196 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32) k_gemv(GemvArgs a) {
 
     // ---------------- consumer warps ----------------
     grid_dep_wait();
-    if (bulk_x) {
-        if (!mbar_wait(sm.x_full, 0, abort_flag, a.err)) *abort_flag = 1;
-    }
-    stage_x<KIND, NCOL>(a, sm.xs, sm.cb, bulk_x ? sm.raw : nullptr, threadIdx.x, NW * 32);
-    named_bar_sync(1, NW * 32);
-
-    int it = 0, gi = 0;
-    for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x, ++gi) {
-        float acc[NCOL];
-#pragma unroll
-        for (int n = 0; n < NCOL; ++n) acc[n] = 0.f;
-        for (int kc = 0; kc < nchunks; ++kc, ++it) {
-            const int s = it % ST, use = it / ST;
-            const bool ok = !*abort_flag && mbar_wait(&sm.full[s], use & 1, abort_flag, a.err);
-            const int units = min(NW, (K - kc * G::CHUNK_E) / G::UNIT_E);
-            if (ok && warp < units)
-                unit<KIND, NCOL>(sm.stage0 + s * G::STAGE_B + lane * G::STRIDE + warp * G::UNIT_B, sm.xs, sm.cb, K,
-                                 kc * G::CHUNK_E + warp * G::UNIT_E, acc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[s]);
-        }
-        // Cross-warp sum through shared memory: every warp deposits its partial
-        // sums and arrives; the group's writer warp (rotating) waits, adds and
-        // stores, then frees the buffer. Only the writer waits.
-        const int p = gi & 1, use = gi >> 1;
-        float* rb = sm.red + p * NCOL * NW * 32;
-        if (use > 0 && !*abort_flag) mbar_wait(&sm.red_empty[p], (use - 1) & 1, abort_flag, a.err);
-#pragma unroll
-        for (int n = 0; n < NCOL; ++n) rb[(n * NW + warp) * 32 + lane] = acc[n];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.red_full[p]);
-        if (warp == gi % NW) {
-            const bool ok = !*abort_flag && mbar_wait(&sm.red_full[p], use & 1, abort_flag, a.err);
-            const int64_t row = g * kRows + lane;
-            if (ok && row < a.M) {
-#pragma unroll
-                for (int n = 0; n < NCOL; ++n) {
-                    if (n < a.ncols) {
-                        float v = 0.f;
-#pragma unroll
-                        for (int w = 0; w < NW; ++w) v += rb[(n * NW + w) * 32 + lane];
-                        a.Y[static_cast<int64_t>(n) * a.M + row] = v;
-                    }
-                }
+    int64_t n_items = rg;
+    if (grouped) {
+        if (!mbar_wait(tbl_ready, 0, abort_flag, a.err)) *abort_flag = 1;
+        n_items = T.misc[0];
+        // assignments with a bad expert id or activation row: NaN rows, flagged
+        if (blockIdx.x == 0 && !*abort_flag && T.misc[1] > 0) {
+            const int nb = T.misc[1], b0 = T.eoff[a.n_experts];
+            for (int64_t idx = threadIdx.x; idx < static_cast<int64_t>(nb) * a.M; idx += NW * 32) {
+                const int64_t j = idx / a.M;
+                a.Y[static_cast<int64_t>(T.order[b0 + j]) * a.M + (idx - j * a.M)] = __int_as_float(0x7fc00000);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.red_empty[p]);
+            if (threadIdx.x == 0) atomicOr(a.err, DEV_ERR_BAD_INDEX);
         }
+    }
+    const int64_t lo = static_cast<int64_t>(blockIdx.x) * n_items / gridDim.x;
+    const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * n_items / gridDim.x;
+    ItemWalker walk;
+    int cur_e = -1, cur_c = -1, it_base = 0, gi = 0;
+    for (int64_t i = lo; i < hi; ++i, it_base += a.cpr, ++gi) {
+        const Item item = walk.at(i, a, T, rg, NCMAX);
+        if (item.e != cur_e || item.col0 != cur_c) {
+            if (cur_e >= 0) named_bar_sync(1, NW * 32);   // everyone is done with the old activations
+            stage_x<KIND, NCMAX>(a, T, item, xs, threadIdx.x, NW * 32);
+            named_bar_sync(1, NW * 32);
+            cur_e = item.e;
+            cur_c = item.col0;
+        }
+        const int nc = item.ncol;
+        if (NCMAX == 1 || nc <= 1)
+            consume_item<KIND, 1, NCMAX>(a, T, item, stage0, stage_b, xs, red, full, empty, red_full, red_empty,
+                                         abort_flag, it_base, gi, warp, lane);
+        else if (NCMAX == 2 || nc <= 2)
+            consume_item<KIND, (NCMAX < 2 ? NCMAX : 2), NCMAX>(a, T, item, stage0, stage_b, xs, red, full, empty,
+                                                               red_full, red_empty, abort_flag, it_base, gi, warp,
+                                                               lane);
+        else if (NCMAX == 4 || nc <= 4)
+            consume_item<KIND, (NCMAX < 4 ? NCMAX : 4), NCMAX>(a, T, item, stage0, stage_b, xs, red, full, empty,
+                                                               red_full, red_empty, abort_flag, it_base, gi, warp,
+                                                               lane);
+        else
+            consume_item<KIND, NCMAX, NCMAX>(a, T, item, stage0, stage_b, xs, red, full, empty, red_full,
+                                             red_empty, abort_flag, it_base, gi, warp, lane);
     }
 }
 
-// Two CTAs per SM: each CTA gets up to half of the SM's shared memory.
-constexpr int kCtaSmem = 113 * 1024;
-
-// Launch tunables, overridable for sweeps: QMM_GEMV_STAGES (2..4) and
-// QMM_GEMV_CTAS (CTAs per SM, 1 or 2). 0 = automatic.
+// Launch tunables, overridable for sweeps: QMM_GEMV_NWU (warps per chunk),
+// QMM_GEMV_STAGES, QMM_GEMV_SMEM (KB of shared memory per CTA), QMM_GEMV_CTAS.
+// 0 = automatic.
 int env_int(const char* name) {
     const char* v = getenv(name);
     return v ? atoi(v) : 0;
 }
+const int kEnvNwu = env_int("QMM_GEMV_NWU");
 const int kEnvStages = env_int("QMM_GEMV_STAGES");
-const int kEnvCtas = env_int("QMM_GEMV_CTAS");
+const int kEnvSmemKB = env_int("QMM_GEMV_SMEM");
+const int kEnvCtas = env_int("QMM_GEMV_CTAS");   // CTAs per SM (1 or 2)
 
-template <int KIND>
-bool ok_kind(const Problem& p) {
-    using G = SGeo<KIND>;
-    if (p.x_row) return false;
-    if (p.N > 8 || p.K > (1 << 24)) return false;
-    if (p.row_bytes % 16 || reinterpret_cast<uintptr_t>(p.W) % 16) return false;
-    if (p.K % G::UNIT_E) return false;
-    if (!G::PARTIAL_OK && p.K % G::CHUNK_E) return false;
-    const int K = static_cast<int>(p.K);
-    if (p.N <= 1) return Smem<KIND, 1>::bytes(K, 2) <= kSmemBudget;
-    if (p.N <= 2) return Smem<KIND, 2>::bytes(K, 2) <= kSmemBudget;
-    if (p.N <= 4) return Smem<KIND, 4>::bytes(K, 2) <= kSmemBudget;
-    return Smem<KIND, 8>::bytes(K, 2) <= kSmemBudget;
+int pow2ceil(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
 }
 
-template <int KIND, int NCOL>
-cudaError_t launch_ncol(const Problem& p, cudaStream_t s) {
+struct Plan {
+    bool ok = false;
+    int ncmax = 1, nwu = 0, stride = 0, stages = 0, upr = 0, cpr = 0;  // stride = box granules * 16
+    size_t smem = 0;
+};
+
+template <int KIND>
+Plan plan(const Problem& p) {
     using G = SGeo<KIND>;
-    const int K = static_cast<int>(p.K);
-    // Prefer two CTAs per SM (more warps to hide latency); otherwise one CTA
-    // with as many stages as fit.
-    // Formats with 8 consumer warps fill an SM with one deep CTA; 4-warp
-    // formats run two CTAs per SM (measured on the decode workload).
-    int stages = kMaxStages, per_sm = 2;
-    while (stages > 2 && Smem<KIND, NCOL>::bytes(K, stages) > kCtaSmem) --stages;
-    const bool one_cta = kEnvCtas == 1 || (kEnvCtas != 2 && G::NW >= 8);
-    if (one_cta || Smem<KIND, NCOL>::bytes(K, stages) > kCtaSmem) {
-        per_sm = 1;
-        stages = kMaxStages;
-        while (stages > 2 && Smem<KIND, NCOL>::bytes(K, stages) > kSmemBudget) --stages;
+    Plan pl;
+    if (p.K > (1 << 24) || p.K % G::UNIT_E) return pl;
+    if (p.row_bytes % 16 || reinterpret_cast<uintptr_t>(p.W) % 16) return pl;
+    const bool grouped = p.x_row != nullptr;
+    if (grouped) {
+        if (p.expert_stride % 16 || p.n_experts > kMaxGroupedExperts || p.N > kMaxGroupedAssign) return pl;
+        const int want = pow2ceil(static_cast<int>((4 * p.N + p.n_experts - 1) / p.n_experts));
+        pl.ncmax = want < 8 ? want : 8;
+        // item counts are int32 on the device
+        if ((p.N + p.n_experts) * ((p.M + kRows - 1) / kRows) >= (int64_t(1) << 31)) return pl;
+    } else {
+        if (p.N > 8) return pl;
+        pl.ncmax = pow2ceil(static_cast<int>(p.N));
     }
-    if (kEnvStages >= 2 && kEnvStages <= kMaxStages &&
-        Smem<KIND, NCOL>::bytes(K, kEnvStages) <= (per_sm == 2 ? kCtaSmem : kSmemBudget))
-        stages = kEnvStages;
-    const size_t smem = Smem<KIND, NCOL>::bytes(K, stages);
-    auto kern = k_gemv<KIND, NCOL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const int K = static_cast<int>(p.K);
+    // Warps per chunk (nwu): a divisor of NW whose chunk is whole 16-byte
+    // vectors, and whose last chunk of a row is too. The NW / nwu consumer
+    // groups take the chunks round-robin, and the number of stages must be a
+    // multiple of the number of groups: then every stage belongs to one group,
+    // which consumes its chunks in order, so no waiter is ever two phases
+    // ahead of a stage's barrier (a parity wait cannot tell those apart).
+    const int E = grouped ? p.n_experts : 0, A = grouped ? static_cast<int>(p.N) : 0;
+    const int pref = (kEnvNwu > 0) ? kEnvNwu : SG<KIND>::NWU;
+    int cands[16], ncand = 0;   // the preferred size, smaller ones, then larger ones
+    for (int w = pref; w >= 1; w >>= 1) cands[ncand++] = w;
+    for (int w = G::NW; w > pref && ncand < 16; w >>= 1) cands[ncand++] = w;
+    for (int ci = 0; ci < ncand; ++ci) {
+        const int w = cands[ci];
+        if (w > G::NW || G::NW % w || (w * G::UNIT_B) % 16) continue;
+        const int upr = K / G::UNIT_E;
+        const int ngroups = G::NW / w;
+        const int cg = w * G::UNIT_B / 16;          // granules per chunk
+        const int bg = (cg % 2) ? cg : cg + 1;      // box granules: odd
+        if (2 * bg > 256) continue;                 // TMA box dimension limit (256 8-byte words)
+        const int stride = bg * 16;
+        const int stage_b = kRows * stride;
+        auto total = [&](int st) { return layout(stage_b, st, pl.ncmax, K, G::NW, grouped, E, A).total; };
+        if (ngroups > kMaxStages || total(ngroups) > kSmemBudget) continue;
+        // two CTAs per SM when the stages fit in half the SM, else one deep CTA
+        const int want = ngroups >= 4 ? ngroups : 4;
+        int budget = kEnvSmemKB > 0 ? kEnvSmemKB * 1024 : (total(want) <= kCoresident ? kCoresident : kSmemBudget);
+        if (budget > kSmemBudget) budget = kSmemBudget;
+        int st = kMaxStages;
+        while (st > ngroups && total(st) > budget) --st;
+        if (kEnvStages > 0 && kEnvStages <= kMaxStages && total(kEnvStages) <= kSmemBudget) st = kEnvStages;
+        st = (st / ngroups) * ngroups;
+        if (st < ngroups) st = ngroups;
+        if (st < 2) st = 2;
+        if (total(st) > kSmemBudget) continue;
+        pl.upr = upr;
+        pl.nwu = w;
+        pl.cpr = (upr + w - 1) / w;
+        pl.stride = stride;
+        pl.stages = st;
+        pl.smem = static_cast<size_t>(total(st));
+        pl.ok = true;
+        return pl;
+    }
+    return pl;
+}
+
+template <int KIND, int NCMAX>
+cudaError_t launch_nc(const Problem& p, const Plan& pl, cudaStream_t s) {
+    using G = SGeo<KIND>;
+    auto kern = k_gemv<KIND, NCMAX>;
+    // weights as (8-byte word of the row, row, expert)
+    CUtensorMap tm;
+    const int E = p.x_row ? p.n_experts : 1;
+    const uint64_t estride = p.x_row ? p.expert_stride : static_cast<uint64_t>(p.M) * p.row_bytes;
+    const uint64_t dims[3] = {p.row_bytes / 8, static_cast<uint64_t>(p.M), static_cast<uint64_t>(E)};
+    const uint64_t strides[2] = {p.row_bytes, estride};
+    const uint32_t box[3] = {static_cast<uint32_t>(pl.stride / 8), static_cast<uint32_t>(kRows), 1};
+    if (!encode_tiled_map(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, p.W, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
     if (e != cudaSuccess) return e;
     int dev = 0;
     cudaGetDevice(&dev);
-    const int64_t ngroups = (p.M + kRows - 1) / kRows;
-    const int grid = static_cast<int>(imin64(ngroups, static_cast<int64_t>(per_sm) * sm_count(dev)));
-    GemvArgs a;
+    const int64_t rg = (p.M + kRows - 1) / kRows;
+    const int sms = sm_count(dev);
+    // plain: at most one CTA per row group; grouped: the item count is known
+    // only on the device, so one CTA per SM
+    const int per_sm = (kEnvCtas == 2 && 2 * pl.smem <= 226 * 1024) ? 2 : 1;
+    const int grid = p.x_row ? per_sm * sms : static_cast<int>(imin64(rg, static_cast<int64_t>(per_sm) * sms));
+    GemvArgs a = {};
     a.W = p.W;
     a.row_bytes = p.row_bytes;
     a.M = p.M;
-    a.K = K;
+    a.K = static_cast<int>(p.K);
     a.X = p.X;
     a.x_dtype = p.x_dtype;
-    a.ncols = static_cast<int>(p.N);
     a.Y = p.Y;
-    a.stages = stages;
+    a.ncols = static_cast<int>(p.N);
+    a.x_row = p.x_row;
+    a.expert_id = p.expert_id;
+    a.expert_stride = p.expert_stride;
+    a.n_experts = p.x_row ? p.n_experts : 0;
+    a.n_assign = p.x_row ? static_cast<int>(p.N) : 0;
+    a.n_x_rows = p.n_x_rows;
+    a.stages = pl.stages;
+    a.nwu = pl.nwu;
+    a.stride = pl.stride;
+    a.upr = pl.upr;
+    a.cpr = pl.cpr;
+    a.flags = (!p.x_row && weight_prefetch()) ? kFlagPrefetchW : 0;
     a.err = p.err;
-    a.flags = (weight_prefetch() ? kFlagPrefetchW : 0) |
-              ((p.x_dtype == 0 && reinterpret_cast<uintptr_t>(p.X) % 16 == 0) ? kFlagBulkX : 0);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3((G::NW + 1) * 32);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, a);
+    e = cudaLaunchKernelEx(&cfg, kern, tm, a);
     count_launch(1);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -634,14 +919,21 @@ cudaError_t launch_ncol(const Problem& p, cudaStream_t s) {
 
 template <int KIND>
 void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
-    if (p.N <= 1) *e = launch_ncol<KIND, 1>(p, s);
-    else if (p.N <= 2) *e = launch_ncol<KIND, 2>(p, s);
-    else if (p.N <= 4) *e = launch_ncol<KIND, 4>(p, s);
-    else *e = launch_ncol<KIND, 8>(p, s);
+    const Plan pl = plan<KIND>(p);
+    if (!pl.ok) {
+        *e = cudaErrorInvalidValue;
+        return;
+    }
+    switch (pl.ncmax) {
+    case 1: *e = launch_nc<KIND, 1>(p, pl, s); break;
+    case 2: *e = launch_nc<KIND, 2>(p, pl, s); break;
+    case 4: *e = launch_nc<KIND, 4>(p, pl, s); break;
+    default: *e = launch_nc<KIND, 8>(p, pl, s); break;
+    }
 }
 
 template <int KIND>
-void ok_dispatch(const Problem& p, bool* out) { *out = ok_kind<KIND>(p); }
+void ok_dispatch(const Problem& p, bool* out) { *out = plan<KIND>(p).ok; }
 
 }  // namespace
 

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qmm {
@@ -24,6 +25,13 @@ bool weight_prefetch();
 
 // Records `n` kernel launches in the process-wide counter.
 void count_launch(int n);
+
+// Encodes a tiled TMA tensor map of `rank` dimensions (dims / box innermost
+// first; strides[i] is the byte stride of dimension i + 1). False when the
+// driver entry point is missing or rejects the description.
+bool encode_tiled_map(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                      const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw,
+                      CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 
 // Problem description shared by the product kernels.
 struct Problem {
@@ -49,7 +57,8 @@ cudaError_t launch_dequant(int kind, const uint8_t* w, int64_t nblocks, float* o
 // k_generic.cu : CUDA-core kernels for any shape and alignment
 cudaError_t launch_generic(const Problem& p, cudaStream_t s);
 
-// k_gemv.cu : weight-streaming GEMV (bulk-copy staged rows), N <= 8 columns
+// k_gemv.cu : weight-streaming GEMV (bulk-copy staged rows): N <= 8 columns, or
+// the expert-grouped product (p.x_row set)
 bool gemv_stream_ok(const Problem& p);
 cudaError_t launch_gemv_stream(const Problem& p, cudaStream_t s);
 

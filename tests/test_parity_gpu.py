@@ -279,3 +279,65 @@ def test_empty_and_refused_shapes(Q):
     with pytest.raises(Q.QmmError) as e:
         Q.qgemm("Q4_0", w, x, 2, 256, 1)
     assert e.value.name == "QMM_ERR_WEIGHTS_TOO_SMALL"
+
+
+# ---------------------------------------------------------------------------
+# degenerate blocks: nonzero scales, every code decoding to a zero weight
+# ---------------------------------------------------------------------------
+def zero_valued_block(kind: str) -> np.ndarray:
+    """One block whose scales are nonzero but whose every element decodes to
+    exactly 0 (the oracle confirms it), so the exact product is 0 and the
+    tolerance is the bare 1e-6: a kernel that cancels a fixed code offset in
+    fp32 (sum (q + c) x - c sum x) would miss it."""
+    bb, _ = synth.block_geometry(kind)
+    b = np.zeros(bb, dtype=np.uint8)
+    d = np.frombuffer(np.float16(3.0e-3).tobytes(), dtype=np.uint8)
+    if kind == "Q8_0":
+        b[0:2] = d                                   # codes 0
+    elif kind == "Q4_0":
+        b[0:2] = d
+        b[2:18] = 0x88                               # q = 8 -> q - 8 = 0
+    elif kind == "Q5_0":
+        b[0:2] = d
+        b[2:6] = 0xFF                                # 5th bit set, low nibbles 0 -> q = 16
+    elif kind in ("Q4_K", "Q5_K"):
+        b[0:2] = d
+        b[2:4] = d                                   # dmin nonzero
+        b[4:8] = 0x05                                # sub-scales 5 (j < 4)
+        b[12:16] = 0x05                              # sub-scales 5 (j >= 4), mins 0
+    elif kind == "Q6_K":
+        b[128:192] = 0xAA                            # high bits 2, low 0 -> q = 32
+        b[192:208] = 3
+        b[208:210] = d
+    elif kind == "Q2_K":
+        b[0:16] = 0x05                               # scale 5, min 0; codes 0
+        b[80:82] = d
+        b[82:84] = d
+    elif kind == "Q3_K":
+        b[0:32] = 0xFF                               # no -4 bias; codes 0
+        b[96:108] = 0x11
+        b[108:110] = d
+    elif kind == "IQ4_XS":
+        b[0:2] = d
+        b[2:4] = 0xAA                                # ls = 32 -> group scale 0
+        b[8:136] = (np.arange(128) * 37 % 256).astype(np.uint8)
+    elif kind == "MXFP4":
+        b[0] = 127
+        b[1:17] = np.tile(np.array([0x00, 0x08, 0x80, 0x88], dtype=np.uint8), 4)  # +0 and -0
+    else:
+        raise ValueError(kind)
+    return b
+
+
+@pytest.mark.parametrize("kind", [k for k in KINDS if k != "IQ4_NL"])
+@pytest.mark.parametrize("N,xdt", [(1, "f32"), (4, "f32"), (33, "f16")])
+def test_zero_valued_codes_with_nonzero_scales(Q, orc, kind, N, xdt):
+    M, K = 96, 4096
+    nb = M * (K // ELEMS[kind])
+    w = np.tile(zero_valued_block(kind), nb)
+    assert not np.any(orc.dequant(kind, w, M, K)), "the hand-built block must decode to zeros"
+    x = synth.activations(N, K, 5 + N, xdt)
+    y, tol = orc.gemm(kind, w, M, K, x, N)
+    Y = sentinel((N, M))
+    Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
+    assert_within(Y.cpu().numpy(), y, tol, f"{kind} zero codes N={N} path={Q.last_path()}")
