@@ -622,15 +622,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Per-group activation sums for the min term: out[n][s][0..G) = hi, [G..2G) = lo
 // with hi = f16(sum), lo = f16(sum - hi); groups of 32 (Q4_K, Q5_K) or 16 (Q2_K).
+// One thread per group, reading its 16 or 32 halves with 16-byte loads (the
+// rows of X are 16-byte aligned and K is a multiple of 256).
 __global__ void k_xsums(const __half* __restrict__ X, int N, int K, int gsize, int G, __half* __restrict__ out) {
     const int ngroups = K / gsize;
     const int64_t total = static_cast<int64_t>(N) * ngroups;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int n = static_cast<int>(i / ngroups), g = static_cast<int>(i % ngroups);
-        const __half* x = X + static_cast<int64_t>(n) * K + static_cast<int64_t>(g) * gsize;
+        const uint4* x = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(n) * K + static_cast<int64_t>(g) * gsize);
+        uint4 v[4];
+        const int nv = gsize / 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (j < nv) v[j] = __ldg(x + j);
         float sum = 0.f;
-        for (int e = 0; e < gsize; ++e) sum += __half2float(x[e]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < nv) {
+                const __half2* h = reinterpret_cast<const __half2*>(&v[j]);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 f = __half22float2(h[t]);
+                    sum += f.x;
+                    sum += f.y;
+                }
+            }
+        }
         const __half hi = __float2half_rn(sum);
         const __half lo = __float2half_rn(sum - __half2float(hi));
         const int s = g / G, gi = g % G;

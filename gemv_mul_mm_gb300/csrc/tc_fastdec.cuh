@@ -324,6 +324,9 @@ template <> struct FastDec<Q5_K> {
 // Q6_K: sub-block j = 2q + hb reads ql[64 (q >> 1) + 32 hb + i] (high nibble
 // when q is odd) and bits 2 (j & 3) .. +1 of qh[128 + 32 (q >> 1) + i];
 // int8 scale per 16 elements at 192 + 2j + i / 16.
+// Four codes at a time: the low nibbles and the two high bits of four
+// elements are merged into four bytes with word-wide shifts and masks, and
+// each byte pair becomes an f16 pair 1024 + code under the 0x64 magic byte.
 template <> struct FastDec<Q6_K> {
     __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
         const int h = q >> 1, nib = q & 1;
@@ -340,13 +343,12 @@ template <> struct FastDec<Q6_K> {
             const int gs = 4 * nib + 2 * hb;   // bit offset of the 2 high bits in qh
 #pragma unroll
             for (int wi = 0; wi < 8; ++wi) {
-                const uint32_t wn = w[wi] >> (4 * nib);
+                // byte k: low nibble from ql, bits 4..5 from qh[k] >> gs
+                const uint32_t hi = ((hq[wi] >> gs) << 4) & 0x30303030u;
+                const uint32_t code = lop_and_or(w[wi] >> (4 * nib), 0x0F0F0F0Fu, hi);
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
-                    const uint32_t sel = p ? 0x4342u : 0x4140u;
-                    const uint32_t x = prmt(hq[wi], 0u, sel) >> gs;
-                    const uint32_t m = lop_and_or(x << 4, 0x00300030u, kMag16);
-                    const uint32_t c = hadd2_u(lop_and_or(prmt(wn, 0u, sel), 0x000F000Fu, m), h2int(-1056));
+                    const uint32_t c = hadd2_u(prmt(code, kMagB, p ? 0x4342u : 0x4140u), h2int(-1056));
                     o[16 * hb + 2 * wi + p] = hmul2_u(c, S[2 * hb + (wi >> 2)]);
                 }
             }
