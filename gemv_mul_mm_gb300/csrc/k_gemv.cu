@@ -205,9 +205,10 @@ __host__ __device__ __forceinline__ int q4_pow(int i) {
     return (i <= 4) ? 4 * i - 16 : 4 * (i - 3) - 16;
 }
 
-// Q4_0: 8 blocks of 18 bytes (144 B, 16-byte aligned in shared memory).
+// Q4_0, one activation column: 8 blocks of 18 bytes (144 B, 16-byte aligned
+// in shared memory), fully unrolled (the fastest form for a single column).
 template <int NC>
-__device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+__device__ __forceinline__ void unit_q4_0_flat(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
     uint32_t w[36];
 #pragma unroll
     for (int i = 0; i < 9; ++i) {
@@ -278,6 +279,78 @@ __device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, int
     }
 }
 
+// Q4_0, several activation columns: the same arithmetic, walked as four pairs
+// of blocks with a rolled loop -- a pair is 36 bytes starting 4-byte aligned
+// (nine 32-bit loads) -- which keeps the multi-column decoder small enough for
+// the instruction cache.
+template <int NC>
+__device__ __forceinline__ void unit_q4_0(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+    const uint32_t mask[5] = {0xFu, 0xF0u, 0xF00u, 0xF000u, 0xF0000u};
+    const uint32_t kMagic = 0x43000000u;   // 128.0f
+    // 128 + 8 * 2^p for the four nibble pairs (0,1) (2,3) (4,5) (6,7)
+    const float2 nb0 = make_float2(-(128.f + 8.f * 0x1p-16f), -(128.f + 8.f * 0x1p-12f));
+    const float2 nb1 = make_float2(-(128.f + 8.f * 0x1p-8f), -(128.f + 8.f * 0x1p-4f));
+    const float2 nb2 = make_float2(-136.f, -(128.f + 8.f * 0x1p-8f));
+    const float2 nb3 = make_float2(-(128.f + 8.f * 0x1p-4f), -136.f);
+#pragma unroll 1
+    for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(u + 36 * pr);
+        uint32_t w[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) w[i] = pw[i];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            // block 2pr (h = 0) starts at the pair's first byte: d in the low
+            // half of word 0, codes 0..1 in its high half, 14..15 in word 4;
+            // block 2pr + 1 (h = 1) has d in the high half of word 4 and its
+            // codes in words 5..8
+            const float d = h2f(h ? (w[4] >> 16) : w[0]);
+            uint32_t words[4];
+            if (h == 0) {
+                words[0] = __byte_perm(w[0], w[4], 0x3254);
+                words[1] = w[1];
+                words[2] = w[2];
+                words[3] = w[3];
+            } else {
+                words[0] = w[5];
+                words[1] = w[6];
+                words[2] = w[7];
+                words[3] = w[8];
+            }
+            const int kb = k0 + 32 * (2 * pr + h);
+            float2 S[NC][2];
+#pragma unroll
+            for (int n = 0; n < NC; ++n) S[n][0] = S[n][1] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t v = words[j], sh = v >> 12;
+                const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[0], kMagic)),
+                                                          __uint_as_float(and_or(v, mask[1], kMagic))), nb0);
+                const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[2], kMagic)),
+                                                          __uint_as_float(and_or(v, mask[3], kMagic))), nb1);
+                const float2 f45 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[4], kMagic)),
+                                                          __uint_as_float(and_or(sh, mask[2], kMagic))), nb2);
+                const float2 f67 = __fadd2_rn(make_float2(__uint_as_float(and_or(sh, mask[3], kMagic)),
+                                                          __uint_as_float(and_or(sh, mask[4], kMagic))), nb3);
+#pragma unroll
+                for (int n = 0; n < NC; ++n) {
+                    const float4 xl = *reinterpret_cast<const float4*>(xs + n * K + kb + 8 * j);
+                    const float4 xh = *reinterpret_cast<const float4*>(xs + n * K + kb + 8 * j + 4);
+                    S[n][0] = __ffma2_rn(f01, make_float2(xl.x, xl.y), S[n][0]);
+                    S[n][1] = __ffma2_rn(f23, make_float2(xl.z, xl.w), S[n][1]);
+                    S[n][0] = __ffma2_rn(f45, make_float2(xh.x, xh.y), S[n][0]);
+                    S[n][1] = __ffma2_rn(f67, make_float2(xh.z, xh.w), S[n][1]);
+                }
+            }
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                const float2 t2 = __fadd2_rn(S[n][0], S[n][1]);
+                acc[n] = fmaf(d, t2.x + t2.y, acc[n]);
+            }
+        }
+    }
+}
+
 // Q8_0: 8 blocks of 34 bytes (272 B). Code byte c (two's complement) XOR 0x80
 // is c + 128; placed in the low byte under 0x4B000000 it reads 2^23 + c + 128,
 // and one packed subtract of (2^23 + 128) leaves c exactly.
@@ -334,7 +407,8 @@ template <int KIND, int NC>
 __device__ __forceinline__ void unit(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
     if constexpr (KIND == Q4_0) {
         static_assert(SG<KIND>::UB == 8, "the Q4_0 decoder takes eight blocks");
-        unit_q4_0<NC>(u, xs, K, k0, acc);
+        if constexpr (NC == 1) unit_q4_0_flat<NC>(u, xs, K, k0, acc);
+        else unit_q4_0<NC>(u, xs, K, k0, acc);
     } else if constexpr (KIND == Q8_0) {
         static_assert(SG<KIND>::UB == 8, "the Q8_0 decoder takes eight blocks");
         unit_q8_0<NC>(u, xs, K, k0, acc);
