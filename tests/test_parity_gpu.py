@@ -341,3 +341,22 @@ def test_zero_valued_codes_with_nonzero_scales(Q, orc, kind, N, xdt):
     Y = sentinel((N, M))
     Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
     assert_within(Y.cpu().numpy(), y, tol, f"{kind} zero codes N={N} path={Q.last_path()}")
+
+
+# ---------------------------------------------------------------------------
+# largest shapes: activations the streaming kernel stages, and past them
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("kind", ["Q4_0", "Q8_0"])
+@pytest.mark.parametrize("K,path", [(32768, "gemv"), (65536, "generic")])
+def test_long_rows_stream_or_fall_back(Q, orc, kind, K, path):
+    """A 32768-element row still has its activations staged in shared memory
+    by the streaming GEMV; a 65536-element row does not fit and must take the
+    generic kernel. Both must match the oracle."""
+    M = 64
+    w = synth.quant_weights(kind, M, K, 31)
+    x = synth.activations(1, K, 32)
+    y, tol = orc.gemm(kind, w, M, K, x, 1)
+    Y = sentinel((1, M))
+    Q.qgemv(kind, dev(w), dev(x), M, K, y=Y.view(-1))
+    assert Q.last_path() == (Q.PATH_GEMV if path == "gemv" else Q.PATH_GENERIC)
+    assert_within(Y.cpu().numpy(), y, tol, f"{kind} K={K}")
