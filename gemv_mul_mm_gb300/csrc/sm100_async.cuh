@@ -93,9 +93,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // Bounded wait for waits on a pipeline's critical path: polls with the cheap
-// test_wait and naps `ns` nanoseconds between probes (a thread suspended in
-// try_wait wakes up late; a tight spin takes issue slots from busy warps).
-// The abort flag and the clock are checked every 16 probes.
+// test_wait, napping `ns` nanoseconds between probes when ns > 0 (a thread
+// suspended in try_wait wakes up late). The abort flag and the clock are
+// checked every 16 probes.
 __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err,
                                                unsigned ns) {
     const long long t0 = clock64();
@@ -103,7 +103,7 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, v
 #pragma unroll 1
         for (int i = 0; i < 16; ++i) {
             if (mbar_test_wait(bar, parity)) return true;
-            __nanosleep(ns);
+            if (ns) __nanosleep(ns);
         }
         if (*abort) return false;
         if (clock64() - t0 > (1ll << 31)) {  // ~1 s at 2 GHz
