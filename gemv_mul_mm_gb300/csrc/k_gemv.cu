@@ -472,9 +472,12 @@ struct Item {
     int64_t g;
 };
 
-// Walks the CTA's contiguous item range in order (plain: one problem).
+// Walks the CTA's contiguous item range in order (plain: one problem). The
+// first lookup binary-searches the expert (a linear scan over up to a thousand
+// experts in shared memory would delay the CTA's first weight copy by
+// microseconds); later ones step forward.
 struct ItemWalker {
-    int e = 0;
+    int e = -1;
     __device__ __forceinline__ Item at(int64_t i, const GemvArgs& a, const Tables& t, int64_t rg, int ncmax) {
         Item it;
         if (!a.x_row) {
@@ -483,6 +486,16 @@ struct ItemWalker {
             it.ncol = a.ncols;
             it.g = i;
             return it;
+        }
+        if (e < 0) {
+            // last expert e with ioff[e] <= i (ioff is non-decreasing, ioff[0] = 0)
+            int lo = 0, hi = a.n_experts;   // ioff[n_experts] = total > i
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (t.ioff[mid] <= i) lo = mid;
+                else hi = mid;
+            }
+            e = lo;
         }
         while (t.ioff[e + 1] <= i) ++e;
         const int64_t local = i - t.ioff[e];
