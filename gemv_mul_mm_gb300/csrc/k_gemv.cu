@@ -614,7 +614,7 @@ __device__ void stage_x(const GemvArgs& a, const Tables& t, const Item& it, floa
 #pragma unroll
         for (int j = 0; j < B; ++j) {
             const int idx = base + j * nthr;
-            if (idx >= total) break;
+            if (idx >= total) continue;   // (no break: the loop must unroll, v[] stays in registers)
             const int n = idx / kq, k = 4 * (idx - n * kq);
             if constexpr (KIND == Q4_0) {
                 const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
@@ -887,8 +887,11 @@ Plan plan(const Problem& p) {
     const bool grouped = p.x_row != nullptr;
     if (grouped) {
         if (p.expert_stride % 16 || p.n_experts > kMaxGroupedExperts || p.N > kMaxGroupedAssign) return pl;
+        // up to four columns per problem: measured on the 64-token MoE
+        // projections, the 8-column decode (register-bound) lost more than
+        // re-streaming the rows of the experts with over four tokens
         const int want = pow2ceil(static_cast<int>((4 * p.N + p.n_experts - 1) / p.n_experts));
-        pl.ncmax = want < 8 ? want : 8;
+        pl.ncmax = want < 4 ? want : 4;
         // item counts are int32 on the device
         if ((p.N + p.n_experts) * ((p.M + kRows - 1) / kRows) >= (int64_t(1) << 31)) return pl;
     } else {
@@ -903,7 +906,10 @@ Plan plan(const Problem& p) {
     // which consumes its chunks in order, so no waiter is ever two phases
     // ahead of a stage's barrier (a parity wait cannot tell those apart).
     const int E = grouped ? p.n_experts : 0, A = grouped ? static_cast<int>(p.N) : 0;
-    const int pref = (kEnvNwu > 0) ? kEnvNwu : SG<KIND>::NWU;
+    // short rows: no more warps per chunk than the row has units (the rest
+    // of a group would idle on every chunk)
+    int pref = (kEnvNwu > 0) ? kEnvNwu : SG<KIND>::NWU;
+    while (pref > 1 && pref > K / G::UNIT_E) pref >>= 1;
     int cands[16], ncand = 0;   // the preferred size, smaller ones, then larger ones
     for (int w = pref; w >= 1; w >>= 1) cands[ncand++] = w;
     for (int w = G::NW; w > pref && ncand < 16; w >>= 1) cands[ncand++] = w;
