@@ -514,22 +514,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&amin_full[b]);
             }
-            for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
-                const int as = sub % AS;
-                // decode first, then wait for the stage to be free: the decode
-                // stays off the stage's round trip (ok is warp-uniform:
-                // tcgen05.st below is warp-collective)
-                uint32_t o[32];
-                if (ok) FastDec<KIND>::sub(row, q, o);
-                if (ok && sub >= AS) ok = warp_wait_bar<true>(&a_empty[as], ((sub / AS) - 1) & 1, abort_flag, a.err);
+            // Two sub-steps per pass: their decodes are independent instruction
+            // streams the compiler interleaves (one decoder warp per scheduler
+            // is latency-bound on a single stream); then each is stored and
+            // published in order. Decode first, then wait for the stage to be
+            // free, so the decode stays off the stage's round trip (ok is
+            // warp-uniform: tcgen05.st is warp-collective).
+            static_assert((KSUP / KSUB) % 2 == 0, "sub-steps are decoded in pairs");
+#pragma unroll 1
+            for (int q = 0; q < KSUP / KSUB; q += 2) {
+                uint32_t o[2][32];
                 if (ok) {
-                    tc_fence_after();
-                    tmem_st32(tmem + lane_addr + as * kACols, o);
-                    tmem_wait_st();
+                    FastDec<KIND>::sub(row, q, o[0]);
+                    FastDec<KIND>::sub(row, q + 1, o[1]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[as]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h, ++sub) {
+                    const int as = sub % AS;
+                    if (ok && sub >= AS)
+                        ok = warp_wait_bar<true>(&a_empty[as], ((sub / AS) - 1) & 1, abort_flag, a.err);
+                    if (ok) {
+                        tc_fence_after();
+                        tmem_st32(tmem + lane_addr + as * kACols, o[h]);
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&a_full[as]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&raw_empty[rs]);
