@@ -321,10 +321,10 @@ def secondary_table(qmm, synth, l2_bytes, stream, pk):
                          "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4), "path": qmm.last_path()}
             del ws
     out["gemm"] = gem
-    # MoE grouped
+    # MoE grouped: both projections of the layer
     moe = {}
-    for T in synth.MOE["tokens"]:
-        p = synth.moe_problem(T, "gate_up")
+    for which, T in [(w, T) for w in ("gate_up", "down") for T in synth.MOE["tokens"]]:
+        p = synth.moe_problem(T, which)
         W = torch.from_numpy(p["w"]).cuda()
         X = torch.from_numpy(p["x"]).cuda()
         xr = torch.from_numpy(p["x_row"]).cuda()
@@ -334,7 +334,7 @@ def secondary_table(qmm, synth, l2_bytes, stream, pk):
                                                   p["M"], p["K"], Y=Y, stream=stream.cuda_stream), 1)
         distinct = len(set(p["expert_id"].tolist()))
         gbs = distinct * p["stride"] / (ms * 1e-3) / 1e9
-        moe[f"gate_up_T{T}"] = {"us": round(ms * 1e3, 2), "distinct_experts": distinct,
+        moe[f"{which}_T{T}"] = {"us": round(ms * 1e3, 2), "distinct_experts": distinct,
                                 "weight_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4)}
         del W
     out["moe_q4_0"] = moe

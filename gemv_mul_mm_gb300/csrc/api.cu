@@ -279,7 +279,7 @@ int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert_stride,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // every touched expert's rows stream once on the GEMV kernel; shapes it
     // does not take (unaligned rows, too many experts) run on the generic one
-    if (g_path.load() != 1 && gemv_stream_ok(p)) return finish(launch_gemv_stream(p, s), 2);
+    if (g_path.load() != 1 && gemv_stream_ok(p)) return finish(launch_gemv_stream(p, s), 5);
     return finish(launch_generic(p, s), 1);
 }
 
@@ -313,6 +313,13 @@ int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X, int x_
     const int r = launch_gemm_tc_noalloc(p, static_cast<cudaStream_t>(stream));
     if (r == QMM_OK) t_last_path = 3;
     return r;
+}
+
+int qmm_selftest_wait_timeout(int64_t cycles, void* stream) {
+    if (cycles < 1 || cycles > (int64_t(1) << 32)) return QMM_ERR_BAD_ARGUMENT;
+    unsigned* err = nullptr;
+    if (int r = err_ptr(&err)) return r;
+    return launch_wait_never(err, cycles, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
 int qmm_check_device_error(void* stream) {

@@ -51,6 +51,9 @@ struct Problem {
     unsigned* err = nullptr; // device latch
 };
 
+// k_selftest.cu : a kernel whose bounded wait runs out (failure-path test)
+cudaError_t launch_wait_never(unsigned* err, long long cycles, cudaStream_t s);
+
 // k_dequant.cu
 cudaError_t launch_dequant(int kind, const uint8_t* w, int64_t nblocks, float* out, cudaStream_t s);
 

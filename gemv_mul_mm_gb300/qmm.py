@@ -31,7 +31,7 @@ STATUS = {
 }
 STATUS_ID = {v: k for k, v in STATUS.items()}
 
-PATH_AUTO, PATH_GENERIC, PATH_GEMV, PATH_TC = 0, 1, 2, 3
+PATH_AUTO, PATH_GENERIC, PATH_GEMV, PATH_TC, PATH_DEQUANT, PATH_GROUPED = 0, 1, 2, 3, 4, 5
 
 
 class QmmError(RuntimeError):
@@ -65,6 +65,7 @@ def _lib():
         L.qgemm_grouped.argtypes = [_I, _P, _SZ, _SZ, _I, _P, _I, _SZ, _I64, _P, _P, _I64,
                                     _P, _SZ, _I64, _I64, _P]
         L.qmm_check_device_error.argtypes = [_P]
+        L.qmm_selftest_wait_timeout.argtypes = [_I64, _P]
         L.qmm_set_path.argtypes = [_I]
         L.qmm_set_weight_prefetch.argtypes = [_I]
         L.qmm_launch_count.restype = ctypes.c_uint64
@@ -194,6 +195,11 @@ def qgemm_grouped(kind, W, expert_stride: int, n_experts: int, X, x_row, expert_
                                 _ptr(expert_id), n_assign, _ptr(Y), Y.numel(), M, K,
                                 _stream(stream)), "qgemm_grouped")
     return Y
+
+
+def selftest_wait_timeout(cycles: int, stream=None):
+    """Queue the failure-path self-test kernel (a bounded wait that runs out)."""
+    _check(_lib().qmm_selftest_wait_timeout(int(cycles), _stream(stream)), "qmm_selftest_wait_timeout")
 
 
 def check_device_error(stream=None) -> int:

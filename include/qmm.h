@@ -220,6 +220,18 @@ QMM_API int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert
  */
 QMM_API int qmm_check_device_error(void* stream);
 
+/*
+ * qmm_selftest_wait_timeout -- test of the failure path (the pages have no
+ * counterpart). Queues on `stream` one small kernel that waits on a shared-
+ * memory barrier nothing ever completes, gives up after `cycles` SM clock
+ * cycles (1 .. 2^32), and latches the same timeout status a real kernel's
+ * bounded wait would. The next qmm_check_device_error() then returns
+ * QMM_ERR_DEVICE_TIMEOUT and clears it; the CUDA context stays usable. No
+ * trap, fault or unbounded wait is involved. Returns QMM_OK, or
+ * QMM_ERR_BAD_ARGUMENT / QMM_ERR_CUDA without launching.
+ */
+QMM_API int qmm_selftest_wait_timeout(int64_t cycles, void* stream);
+
 /* Kernel-path override, for tests and experiments: 0 = automatic (default),
  * 1 = force the generic CUDA-core kernels, 2 = force the streaming GEMV for
  * qgemm (N <= 8), 3 = force the tensor-core GEMM for qgemm. Returns the

@@ -112,3 +112,9 @@ def test_path_override(L):
     assert qmm.set_path(0) == 1
     assert qmm.set_path(9) == -1
     assert qmm.set_path(0) == 0
+
+
+def test_selftest_refuses_bad_cycle_counts(L):
+    import ctypes
+    for bad in (0, -5, (1 << 32) + 1):
+        assert L.qmm_selftest_wait_timeout(ctypes.c_int64(bad), None) == 13   # QMM_ERR_BAD_ARGUMENT

@@ -360,3 +360,22 @@ def test_long_rows_stream_or_fall_back(Q, orc, kind, K, path):
     Q.qgemv(kind, dev(w), dev(x), M, K, y=Y.view(-1))
     assert Q.last_path() == (Q.PATH_GEMV if path == "gemv" else Q.PATH_GENERIC)
     assert_within(Y.cpu().numpy(), y, tol, f"{kind} K={K}")
+
+
+# ---------------------------------------------------------------------------
+# failure path: a bounded wait that runs out is reported, the context survives
+# ---------------------------------------------------------------------------
+def test_device_timeout_is_reported_and_context_survives(Q, orc):
+    assert Q.check_device_error() == 0
+    Q.selftest_wait_timeout(1 << 22)           # a few milliseconds of waiting
+    assert Q.check_device_error() == Q.STATUS_ID["QMM_ERR_DEVICE_TIMEOUT"]
+    assert Q.check_device_error() == 0         # the latch was cleared
+    # the context is still usable: a GEMV right after matches the oracle
+    M, K = 96, 1024
+    w = synth.quant_weights("Q8_0", M, K, 51)
+    x = synth.activations(1, K, 52)
+    y, tol = orc.gemm("Q8_0", w, M, K, x, 1)
+    Y = sentinel((1, M))
+    Q.qgemv("Q8_0", dev(w), dev(x), M, K, y=Y.view(-1))
+    assert_within(Y.cpu().numpy(), y, tol, "after timeout")
+    assert Q.check_device_error() == 0
