@@ -190,18 +190,6 @@ __device__ __forceinline__ float2 scale256(const uint8_t* b) {
     else return make_float2(h2f(ld16(b, 0)), 0.f);  // IQ4_XS
 }
 
-// Min code of group g (Q4_K/Q5_K: 8 groups of 32; Q2_K: 16 groups of 16).
-template <int KIND>
-__device__ __forceinline__ float min_code(const uint8_t* b, int g) {
-    if constexpr (KIND == Q2_K) {
-        return static_cast<float>(b[g] >> 4);
-    } else {
-        int sc, mn;
-        k4_sm(b + 4, g, sc, mn);
-        return static_cast<float>(mn);
-    }
-}
-
 // Runtime kind -> template dispatch helper.
 #define QMM_DISPATCH_KIND(kind, FN, ...)                          \
     switch (kind) {                                               \

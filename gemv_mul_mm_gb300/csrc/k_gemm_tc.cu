@@ -182,10 +182,6 @@ __device__ __forceinline__ bool bar_red_and(int id, int nthreads, bool v) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 // Bounded wait that also honours the CTA's abort flag; false = give up.
 // A phase that has already completed is taken without touching the flag.
@@ -226,6 +222,39 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, unsign
             atomicOr(err, DEV_ERR_TIMEOUT);
             return;
         }
+    }
+}
+
+// The 16 f16 min codes of one A_min tile row as eight f16x2 words, extracted
+// with word-wide masks and shifts and made exact f16 by the 0x64 magic byte
+// (1024 + m, minus 1024): Q4_K / Q5_K -- the 8 mins of the 12-byte scale field
+// (bytes 4..7 low 6 bits; bytes 8..11 high nibble with the top 2 bits of bytes
+// 4..7), twice; Q2_K -- the high nibbles of its 16 scale bytes. The row's
+// scale field is 4-byte aligned in the staged tile for all three formats.
+template <int KIND>
+__device__ __forceinline__ void min_words(const uint8_t* row, uint32_t (&w)[8]) {
+    const uint32_t m1024 = h2int(-1024);
+    if constexpr (KIND == Q2_K) {
+        const uint32_t* f = reinterpret_cast<const uint32_t*>(row);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t m4 = (f[i] >> 4) & 0x0F0F0F0Fu;
+            w[2 * i] = hadd2_u(prmt(m4, kMagB, 0x4140u), m1024);
+            w[2 * i + 1] = hadd2_u(prmt(m4, kMagB, 0x4342u), m1024);
+        }
+    } else {
+        const uint32_t* f = reinterpret_cast<const uint32_t*>(row + 4);
+        const uint32_t s1 = f[1], s2 = f[2];
+        const uint32_t lo4 = s1 & 0x3F3F3F3Fu;
+        const uint32_t hi4 = ((s2 >> 4) & 0x0F0F0F0Fu) | (((s1 >> 6) & 0x03030303u) << 4);
+        w[0] = hadd2_u(prmt(lo4, kMagB, 0x4140u), m1024);
+        w[1] = hadd2_u(prmt(lo4, kMagB, 0x4342u), m1024);
+        w[2] = hadd2_u(prmt(hi4, kMagB, 0x4140u), m1024);
+        w[3] = hadd2_u(prmt(hi4, kMagB, 0x4342u), m1024);
+        w[4] = w[0];
+        w[5] = w[1];
+        w[6] = w[2];
+        w[7] = w[3];
     }
 }
 
@@ -496,14 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && s >= 2) ok = warp_wait_bar(&amin_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err);
                 if (ok) {
                     // A_min tile(s): 32B-swizzled K-major, 16 f16 per row per tile
+                    // (every tile holds the same min codes: they meet the hi
+                    // and the lo halves of the activation sums)
+                    uint32_t w[8];
+                    min_words<KIND>(row, w);
 #pragma unroll
                     for (int t = 0; t < MN::TILES; ++t) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            const int g0 = (MN::G == 8) ? (e & 7) : e, g1 = (MN::G == 8) ? ((e + 1) & 7) : e + 1;
-                            w[e / 2] = pack_h2(min_code<KIND>(row, g0), min_code<KIND>(row, g1));
-                        }
                         uint8_t* tb = amin + b * L::MINB + t * MIN_TILE + (r >> 3) * 256 + (r & 7) * 32;
                         const int sw = (r >> 2) & 1;
                         *reinterpret_cast<uint4*>(tb + ((0 ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
