@@ -548,12 +548,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // free, so the decode stays off the stage's round trip (ok is
             // warp-uniform: tcgen05.st is warp-collective).
             static_assert((KSUP / KSUB) % 2 == 0, "sub-steps are decoded in pairs");
+            // K-quants: the super-block's integer sub-scales as f16, once
+            uint32_t scw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            if constexpr (FastDecPre<KIND>::ON) {
+                if (ok) FastDec<KIND>::pre(row, scw);
+            }
 #pragma unroll 1
             for (int q = 0; q < KSUP / KSUB; q += 2) {
                 uint32_t o[2][32];
                 if (ok) {
-                    FastDec<KIND>::sub(row, q, o[0]);
-                    FastDec<KIND>::sub(row, q + 1, o[1]);
+                    if constexpr (FastDecPre<KIND>::ON) {
+                        FastDec<KIND>::sub_pre(row, q, o[0], scw);
+                        FastDec<KIND>::sub_pre(row, q + 1, o[1], scw);
+                    } else {
+                        FastDec<KIND>::sub(row, q, o[0]);
+                        FastDec<KIND>::sub(row, q + 1, o[1]);
+                    }
                 }
 #pragma unroll
                 for (int h = 0; h < 2; ++h, ++sub) {

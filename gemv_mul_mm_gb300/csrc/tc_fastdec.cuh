@@ -7,7 +7,10 @@
 // applied to the partial sums in the epilogue, not here.
 //
 // Output: o[e / 2] holds elements e and e + 1 of the sub-step (e even) as an
-// f16x2 word, low half = element e. The GEMM stores o[4c .. 4c + 3] as the
+// f16x2 word, low half = element e. The K-quants (FastDecPre) split the work:
+// pre() turns the super-block's integer sub-scales into f16 words once,
+// sub_pre() decodes a sub-step with them; the other formats decode a sub-step
+// with sub(). The GEMM stores o[4c .. 4c + 3] as the
 // 16-byte chunk c (elements 8c .. 8c + 7) of the row's K-major operand row.
 //
 // Techniques (no per-element conversions, no table loads from memory):
@@ -146,6 +149,10 @@ __device__ __forceinline__ void ld_words(const uint8_t* p, uint32_t (&w)[NW]) {
 }
 
 template <int KIND> struct FastDec;
+// Formats whose decoder takes per-super-block scale words (pre / sub_pre).
+template <int KIND> struct FastDecPre {
+    static constexpr bool ON = KIND == Q4_K || KIND == Q5_K || KIND == Q6_K || KIND == Q2_K || KIND == Q3_K;
+};
 
 // ---------------------------------------------------------------------------
 // 32-element formats: sub-step q covers blocks 2q and 2q + 1 of the super-step.
@@ -272,14 +279,54 @@ template <> struct FastDec<IQ4_XS> {
     }
 };
 
+// Q4_K / Q5_K integer sub-scales, once per super-block: the eight 6-bit
+// scales of the 12-byte field (bytes 0..3 low 6 bits; bytes 8..11 low nibble
+// with the top 2 bits of bytes 0..3), extracted word-wide and made exact f16
+// pairs (1024 + sc under the 0x64 magic byte, minus 1024): scw[i] holds the
+// scales of sub-blocks 2i and 2i + 1.
+__device__ __forceinline__ void k4_scale_words(const uint8_t* row, uint32_t (&scw)[8]) {
+    const uint32_t* f = reinterpret_cast<const uint32_t*>(row + 4);   // 4-byte aligned in the stage
+    const uint32_t s0 = f[0], s2 = f[2];
+    const uint32_t lo4 = s0 & 0x3F3F3F3Fu;
+    const uint32_t hi4 = (s2 & 0x0F0F0F0Fu) | (((s0 >> 6) & 0x03030303u) << 4);
+    scw[0] = hadd2_u(prmt(lo4, kMagB, 0x4140u), h2int(-1024));
+    scw[1] = hadd2_u(prmt(lo4, kMagB, 0x4342u), h2int(-1024));
+    scw[2] = hadd2_u(prmt(hi4, kMagB, 0x4140u), h2int(-1024));
+    scw[3] = hadd2_u(prmt(hi4, kMagB, 0x4342u), h2int(-1024));
+}
+
+// The four f16x2 operands of sub-step q from the scale words: the low
+// sub-block's scale sc0 (a0 = sc0, b0 = -1024 sc0) and the high one's
+// (a1 = sc1 / 16, b1 = -64 sc1), all exact in f16.
+__device__ __forceinline__ void k4_sub_operands(const uint32_t (&scw)[8], int q, uint32_t& a0, uint32_t& b0,
+                                                uint32_t& a1, uint32_t& b1) {
+    const uint32_t w = q == 0 ? scw[0] : q == 1 ? scw[1] : q == 2 ? scw[2] : scw[3];
+    a0 = prmt(w, w, 0x1010u);
+    const uint32_t s1 = prmt(w, w, 0x3232u);
+    b0 = hmul2_u(a0, h2int(-1024));
+    a1 = hmul2_u(s1, kH2Sixteenth);
+    b1 = hmul2_u(s1, h2int(-64));
+}
+
+// The four per-16-element scales of sub-step q (groups 4q .. 4q + 3) from
+// eight precomputed f16x2 words, each duplicated into both halves.
+__device__ __forceinline__ void group_scales(const uint32_t (&scw)[8], int q, uint32_t (&S)[4]) {
+    const uint32_t w0 = q == 0 ? scw[0] : q == 1 ? scw[2] : q == 2 ? scw[4] : scw[6];
+    const uint32_t w1 = q == 0 ? scw[1] : q == 1 ? scw[3] : q == 2 ? scw[5] : scw[7];
+    S[0] = prmt(w0, w0, 0x1010u);
+    S[1] = prmt(w0, w0, 0x3232u);
+    S[2] = prmt(w1, w1, 0x1010u);
+    S[3] = prmt(w1, w1, 0x3232u);
+}
+
 // Q4_K: code bytes 16 + 32q .. +32; low nibbles are sub-block 2q, high 2q + 1.
 template <> struct FastDec<Q4_K> {
-    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
-        int sc0, m0, sc1, m1;
-        k4_sm(row + 4, 2 * q, sc0, m0);
-        k4_sm(row + 4, 2 * q + 1, sc1, m1);
-        const uint32_t a0 = h2dup(static_cast<float>(sc0)), b0 = h2dup(-1024.f * sc0);
-        const uint32_t a1 = h2dup(0.0625f * sc1), b1 = h2dup(-64.f * sc1);
+    __device__ __forceinline__ static void pre(const uint8_t* row, uint32_t (&scw)[8]) { k4_scale_words(row, scw); }
+    // sub-step q with the super-block's scale words precomputed
+    __device__ __forceinline__ static void sub_pre(const uint8_t* row, int q, uint32_t (&o)[32],
+                                                   const uint32_t (&scw)[8]) {
+        uint32_t a0, b0, a1, b1;
+        k4_sub_operands(scw, q, a0, b0, a1, b1);
         uint32_t w[8];
         ld_words<8, 16>(row + 16 + 32 * q, w);
 #pragma unroll
@@ -296,12 +343,12 @@ template <> struct FastDec<Q4_K> {
 // Q5_K: as Q4_K with code bytes at 48 + 32q and the 5th bit of element i of
 // sub-block j in bit j of qh[i] (qh at byte 16).
 template <> struct FastDec<Q5_K> {
-    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
-        int sc0, m0, sc1, m1;
-        k4_sm(row + 4, 2 * q, sc0, m0);
-        k4_sm(row + 4, 2 * q + 1, sc1, m1);
-        const uint32_t a0 = h2dup(static_cast<float>(sc0)), b0 = h2dup(-1024.f * sc0);
-        const uint32_t a1 = h2dup(0.0625f * sc1), b1 = h2dup(-64.f * sc1);
+    __device__ __forceinline__ static void pre(const uint8_t* row, uint32_t (&scw)[8]) { k4_scale_words(row, scw); }
+    // sub-step q with the super-block's scale words precomputed
+    __device__ __forceinline__ static void sub_pre(const uint8_t* row, int q, uint32_t (&o)[32],
+                                                   const uint32_t (&scw)[8]) {
+        uint32_t a0, b0, a1, b1;
+        k4_sub_operands(scw, q, a0, b0, a1, b1);
         uint32_t w[8], h[8];
         ld_words<8, 16>(row + 48 + 32 * q, w);
         ld_words<8, 16>(row + 16, h);
@@ -328,22 +375,31 @@ template <> struct FastDec<Q5_K> {
 // elements are merged into four bytes with word-wide shifts and masks, and
 // each byte pair becomes an f16 pair 1024 + code under the 0x64 magic byte.
 template <> struct FastDec<Q6_K> {
-    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
-        const int h = q >> 1, nib = q & 1;
-        uint32_t sw[1], hq[8];
-        ld_words<1, 2>(row + 192 + 4 * q, sw);
-        ld_words<8, 2>(row + 128 + 32 * h, hq);
-        uint32_t S[4];
+    // the sixteen int8 scales (bytes 192..207) as exact f16: byte ^ 0x80
+    // under the 0x64 magic byte is 1024 + b + 128, minus 1152
+    __device__ __forceinline__ static void pre(const uint8_t* row, uint32_t (&scw)[8]) {
+        uint32_t sw[4];
+        ld_words<4, 2>(row + 192, sw);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) S[k] = h2dup(static_cast<float>(static_cast<int8_t>(sw[0] >> (8 * k))));
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t u = sw[i] ^ 0x80808080u;
+            scw[2 * i] = hadd2_u(prmt(u, kMagB, 0x4140u), h2int(-1152));
+            scw[2 * i + 1] = hadd2_u(prmt(u, kMagB, 0x4342u), h2int(-1152));
+        }
+    }
+    __device__ __forceinline__ static void sub_pre(const uint8_t* row, int q, uint32_t (&o)[32],
+                                                   const uint32_t (&scw)[8]) {
+        const int h = q >> 1, nib = q & 1;
+        uint32_t hq[8], S[4];
+        ld_words<8, 2>(row + 128 + 32 * h, hq);
+        group_scales(scw, q, S);
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
             uint32_t w[8];
             ld_words<8, 2>(row + 64 * h + 32 * hb, w);
-            const int gs = 4 * nib + 2 * hb;   // bit offset of the 2 high bits in qh
+            const int gs = 4 * nib + 2 * hb;
 #pragma unroll
             for (int wi = 0; wi < 8; ++wi) {
-                // byte k: low nibble from ql, bits 4..5 from qh[k] >> gs
                 const uint32_t hi = ((hq[wi] >> gs) << 4) & 0x30303030u;
                 const uint32_t code = lop_and_or(w[wi] >> (4 * nib), 0x0F0F0F0Fu, hi);
 #pragma unroll
@@ -359,17 +415,24 @@ template <> struct FastDec<Q6_K> {
 // Q2_K: sub-block j = 2q + hb reads bits 2 (j & 3) .. +1 of qs[16 + 32 (q >> 1) + i];
 // 4-bit scale per 16 elements in the low nibble of byte 2j + i / 16.
 template <> struct FastDec<Q2_K> {
-    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
-        uint32_t sw[1], w[8];
-        ld_words<1, 4>(row + 4 * q, sw);
-        ld_words<8, 4>(row + 16 + 32 * (q >> 1), w);
-        uint32_t A[4], B[4];
+    // the sixteen 4-bit scales (low nibbles of bytes 0..15) as exact f16
+    __device__ __forceinline__ static void pre(const uint8_t* row, uint32_t (&scw)[8]) {
+        uint32_t sw[4];
+        ld_words<4, 4>(row, sw);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float s = static_cast<float>((sw[0] >> (8 * k)) & 15u);
-            A[k] = h2dup(s);
-            B[k] = h2dup(-1024.f * s);
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t m = sw[i] & 0x0F0F0F0Fu;
+            scw[2 * i] = hadd2_u(prmt(m, kMagB, 0x4140u), h2int(-1024));
+            scw[2 * i + 1] = hadd2_u(prmt(m, kMagB, 0x4342u), h2int(-1024));
         }
+    }
+    __device__ __forceinline__ static void sub_pre(const uint8_t* row, int q, uint32_t (&o)[32],
+                                                   const uint32_t (&scw)[8]) {
+        uint32_t w[8], A[4], B[4];
+        ld_words<8, 4>(row + 16 + 32 * (q >> 1), w);
+        group_scales(scw, q, A);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) B[k] = hmul2_u(A[k], h2int(-1024));
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
             const int gs = 4 * (q & 1) + 2 * hb;
@@ -389,13 +452,27 @@ template <> struct FastDec<Q2_K> {
 // Q3_K: sub-block j = 2q + hb reads bits 2 (j & 3) .. +1 of qs[32 + 32 (q >> 1) + i]
 // and bit j of hmask[i] (clear = subtract 4); 6-bit scale per 16 elements.
 template <> struct FastDec<Q3_K> {
-    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
-        uint32_t hm[8], w[8];
+    // the sixteen 6-bit scales of the 12-byte field at 96, minus 32, as exact
+    // f16: low nibbles from bytes 0..7 (low / high halves), the 2 high bits
+    // from bytes 8..11 shifted by 2 per group of four
+    __device__ __forceinline__ static void pre(const uint8_t* row, uint32_t (&scw)[8]) {
+        uint32_t f[3];
+        ld_words<3, 2>(row + 96, f);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint32_t lo = (g == 0) ? (f[0] & 0x0F0F0F0Fu) : (g == 1) ? (f[1] & 0x0F0F0F0Fu)
+                              : (g == 2) ? ((f[0] >> 4) & 0x0F0F0F0Fu) : ((f[1] >> 4) & 0x0F0F0F0Fu);
+            const uint32_t code = lo | (((f[2] >> (2 * g)) & 0x03030303u) << 4);
+            scw[2 * g] = hadd2_u(prmt(code, kMagB, 0x4140u), h2int(-1056));
+            scw[2 * g + 1] = hadd2_u(prmt(code, kMagB, 0x4342u), h2int(-1056));
+        }
+    }
+    __device__ __forceinline__ static void sub_pre(const uint8_t* row, int q, uint32_t (&o)[32],
+                                                   const uint32_t (&scw)[8]) {
+        uint32_t hm[8], w[8], S[4];
         ld_words<8, 2>(row, hm);
         ld_words<8, 2>(row + 32 + 32 * (q >> 1), w);
-        uint32_t S[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) S[k] = h2dup(static_cast<float>(q3_scale(row + 96, 4 * q + k) - 32));
+        group_scales(scw, q, S);
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
             const int j = 2 * q + hb;
@@ -407,7 +484,6 @@ template <> struct FastDec<Q3_K> {
                     const uint32_t sel = p ? 0x4342u : 0x4140u;
                     const uint32_t mk = lop_and_or(prmt(hm[wi], 0u, sel) >> j << 2, 0x00040004u, kMag16);
                     const uint32_t c16 = lop_and_or(prmt(w[wi], 0u, sel) >> gs, 0x00030003u, mk);
-                    // 1024 + q2 + 4 hbit - 1028 = q2 - (hbit ? 0 : 4)
                     o[16 * hb + 2 * wi + p] = hmul2_u(hadd2_u(c16, h2int(-1028)), S[2 * hb + (wi >> 2)]);
                 }
             }
