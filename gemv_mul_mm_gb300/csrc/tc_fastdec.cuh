@@ -7,7 +7,7 @@
 // applied to the partial sums in the epilogue, not here.
 //
 // Output: o[e / 2] holds elements e and e + 1 of the sub-step (e even) as an
-// f16x2 word, low half = element e. The K-quants (FastDecPre) split the work:
+// f16x2 word, low half = element e. The K-quants and IQ4_XS (FastDecPre) split the work:
 // pre() turns the super-block's integer sub-scales into f16 words once,
 // sub_pre() decodes a sub-step with them; the other formats decode a sub-step
 // with sub(). The GEMM stores o[4c .. 4c + 3] as the
@@ -151,7 +151,8 @@ __device__ __forceinline__ void ld_words(const uint8_t* p, uint32_t (&w)[NW]) {
 template <int KIND> struct FastDec;
 // Formats whose decoder takes per-super-block scale words (pre / sub_pre).
 template <int KIND> struct FastDecPre {
-    static constexpr bool ON = KIND == Q4_K || KIND == Q5_K || KIND == Q6_K || KIND == Q2_K || KIND == Q3_K;
+    static constexpr bool ON =
+        KIND == Q4_K || KIND == Q5_K || KIND == Q6_K || KIND == Q2_K || KIND == Q3_K || KIND == IQ4_XS;
 };
 
 // ---------------------------------------------------------------------------
@@ -263,18 +264,34 @@ template <> struct FastDec<MXFP4> {
 // 256-element formats: sub-step q covers 32-element sub-blocks 2q and 2q + 1.
 // ---------------------------------------------------------------------------
 template <> struct FastDec<IQ4_XS> {
-    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
+    // the eight 6-bit group scales minus 32 as exact f16: low nibbles from
+    // scales_l (even groups low, odd groups high nibble of each byte), the two
+    // high bits from scales_h spread one nibble per byte. scw[0..1] hold the
+    // even groups (0, 2), (4, 6); scw[2..3] the odd ones (1, 3), (5, 7).
+    __device__ __forceinline__ static void pre(const uint8_t* row, uint32_t (&scw)[8]) {
         uint32_t hdr[2];   // d | scales_h << 16, scales_l
         ld_words<2, 8>(row, hdr);
+        const uint32_t sh = hdr[0] >> 16, sl = hdr[1];
+        const uint32_t t = (sh & 0xFu) | ((sh & 0xF0u) << 4) | ((sh & 0xF00u) << 8) | ((sh & 0xF000u) << 12);
+        const uint32_t ce = (sl & 0x0F0F0F0Fu) | ((t & 0x03030303u) << 4);
+        const uint32_t co = ((sl >> 4) & 0x0F0F0F0Fu) | (((t >> 2) & 0x03030303u) << 4);
+        scw[0] = hadd2_u(prmt(ce, kMagB, 0x4140u), h2int(-1056));
+        scw[1] = hadd2_u(prmt(ce, kMagB, 0x4342u), h2int(-1056));
+        scw[2] = hadd2_u(prmt(co, kMagB, 0x4140u), h2int(-1056));
+        scw[3] = hadd2_u(prmt(co, kMagB, 0x4342u), h2int(-1056));
+    }
+    __device__ __forceinline__ static void sub_pre(const uint8_t* row, int q, uint32_t (&o)[32],
+                                                   const uint32_t (&scw)[8]) {
+        const uint32_t sel = (q & 1) ? 0x3232u : 0x1010u;
+        const uint32_t we = (q < 2) ? scw[0] : scw[1], wo = (q < 2) ? scw[2] : scw[3];
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
             const int j = 2 * q + hb;
-            const int ls = static_cast<int>(((hdr[1] >> (4 * j)) & 15u) | (((hdr[0] >> (16 + 2 * j)) & 3u) << 4));
-            const float sc = static_cast<float>(ls - 32);
+            const uint32_t sc = prmt(hb ? wo : we, hb ? wo : we, sel);
             uint32_t w[4];
             ld_words<4, 8>(row + 8 + 16 * j, w);
             // (1024 + b) * sc - 1152 * sc = KV * sc, one rounding
-            lut_block<KvTable, kMagB, 0u>(w, h2dup(sc), h2dup(-1152.f * sc), true, o + 16 * hb);
+            lut_block<KvTable, kMagB, 0u>(w, sc, hmul2_u(sc, h2int(-1152)), true, o + 16 * hb);
         }
     }
 };
