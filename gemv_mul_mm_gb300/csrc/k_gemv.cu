@@ -3,17 +3,17 @@
 //
 // y[n, m] = sum_k W[m, k] * x[n, k] for up to 8 activation rows, and the
 // expert-indexed form where output row r reads expert expert_id[r]'s weights
-// and activation row x_row[r]. Decode is bound by streaming the weights from
-// HBM once (inferencelayer 0.2.8 src/cublas_prefill.rs: "decode's whole cost
-// is streaming weights"), so the design is about bytes in flight, coalescing
-// and a lean decode:
+// and activation row x_row[r]. A decode-time GEMV spends its time reading the
+// weights from HBM, once (the `Q4_GEMV_KERNEL` notes of inferencelayer 0.2.8
+// src/cublas_prefill.rs make the same point), so the design is about bytes in
+// flight, coalescing and a lean decode:
 //
 //   * Work items are groups of 32 weight rows (one row per lane) of one
 //     "problem": the plain product is one problem; the grouped product has one
-//     problem per (expert, block of up to NCMAX assignments of that expert), so
-//     every touched expert's rows stream from HBM once however many tokens
-//     chose it. Each CTA (persistent, one per SM) takes a contiguous, equal
-//     share of the items.
+//     problem per (expert, block of up to NCMAX <= 4 assignments of that
+//     expert), so an expert's rows stream from HBM once per block of its
+//     tokens (once for most experts), not once per token. Each CTA
+//     (persistent, one per SM) takes a contiguous, equal share of the items.
 //   * One producer thread moves K-chunks of an item's 32 rows from HBM into a
 //     ring of shared-memory stages, one TMA tensor copy per stage
 //     (`cp.async.bulk.tensor.3d`, completing on an mbarrier, L2 evict-first).

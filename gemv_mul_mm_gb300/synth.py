@@ -2,9 +2,9 @@
 
 This module draws bytes and numbers; it holds none of the method's arithmetic
 (no decoding of any block format). It knows only where each format keeps its
-f16 scale fields, so that it can overwrite them with a bounded distribution, as
-the Vulkore quant_test.cpp harness does in `random_blocks` ("random BYTES ...
-with the fp16 scale fields forced into a sane range").
+f16 scale fields, so that it can overwrite them with a bounded distribution --
+the same idea as the Vulkore quant_test.cpp harness's `random_blocks`, which
+fills blocks with random bytes and then bounds their scale fields.
 
 Generator: splitmix64 (Steele, Lea & Flood, "Fast splittable pseudorandom number
 generators", OOPSLA 2014), counter-based, so any slice can be regenerated.

@@ -25,7 +25,8 @@
  *     qmm_check_device_error().
  *   - There is no fallback to a different computation and no CPU path: a format
  *     this library does not implement is QMM_ERR_BAD_KIND (ferrox-cuda
- *     mul_mm.rs, `kind_by_name`: the caller must fall back and say so).
+ *     mul_mm.rs, `kind_by_name`: an unknown format is reported to the caller,
+ *     who chooses another implementation).
  *   - Every output element is written exactly once per call (no accumulation
  *     into the output), so sentinel-prefilled outputs are fully overwritten.
  */
@@ -128,7 +129,7 @@ QMM_API int qdequant(int kind, const void* blocks, size_t blocks_bytes, int64_t 
 /*
  * qgemv -- decode GEMV, y[m] = sum_k W[m, k] * x[k] (one activation row).
  * Exactly qgemm with N = 1 (inferencelayer 0.2.8 src/cublas_prefill.rs,
- * `Q4_GEMV_KERNEL`: the decode-side GEMV whose whole cost is streaming weights).
+ * `Q4_GEMV_KERNEL`: the decode-time GEMV, bound by reading the weights).
  *
  *   W        device, M * row_bytes bytes, any alignment (16-byte aligned W with
  *            16-byte-multiple rows takes the streaming fast path)
@@ -197,6 +198,13 @@ QMM_API int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X
  *
  * where W_e = W + e * expert_stride bytes holds expert e's M x K weights. Each
  * assignment writes its own output row (no top-k combine).
+ *
+ * On the weight-streaming kernel, the assignments are bucketed by expert on
+ * the device. Every touched expert's rows are then read from memory once per
+ * block of up to four of its assignments. That kernel needs 16-byte aligned W,
+ * expert_stride and row bytes multiples of 16, n_experts <= 1024 and
+ * n_assign <= 4096. Other shapes run on the generic kernel, one pass per
+ * assignment. Accuracy is as for qgemm.
  *
  *   W               device, n_experts experts of M rows each; w_bytes its size
  *   expert_stride   bytes between experts (>= M * row_bytes)

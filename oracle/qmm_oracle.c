@@ -33,8 +33,9 @@
  * Formats and their page of origin:
  *   Q8_0, Q5_0, Q4_K, Q6_K    Vulkore quant_test.cpp, namespace `ref`.
  *   Q4_0                      ferrox-cuda codebook.rs, `IQ4_NL` doc comment
- *                             (Q4_0's packing: low nibble of byte j is element
- *                             j, high nibble element j+16, with a -8 bias).
+ *                             (Q4_0's packing: code byte j holds element j in
+ *                             its low four bits and element j+16 in its high
+ *                             four bits; codes carry a -8 bias).
  *   IQ4_NL, IQ4_XS, MXFP4     ferrox-cuda codebook.rs, the three kind rows and
  *                             the `KVALUES_IQ4NL` / `KVALUES_MXFP4` tables.
  *   Q5_K, Q2_K, Q3_K          named by ferrox-cuda mul_mm.rs (module docs and

@@ -102,8 +102,8 @@ def check_scalar_golden(orc):
 # codebooks by decode (ferrox-cuda 0.20.0 codebook.rs tests)
 # ---------------------------------------------------------------------------
 def check_iq4nl_codebook(orc):
-    """d = 1.0 and byte j = code j in both nibbles: the block decodes to the
-    codebook twice over (low nibbles first)."""
+    """d = 1.0 and byte j = code j in both nibbles: elements 0..15 and again
+    16..31 must read the 16 table values in order."""
     table = [float(v) for _, v in load_table("iq4nl_codebook.txt")]
     b = blk("IQ4_NL")
     b[0], b[1] = ONE
