@@ -379,3 +379,37 @@ def test_device_timeout_is_reported_and_context_survives(Q, orc):
     Q.qgemv("Q8_0", dev(w), dev(x), M, K, y=Y.view(-1))
     assert_within(Y.cpu().numpy(), y, tol, "after timeout")
     assert Q.check_device_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# grouped product: limits of the streaming kernel, crowded experts, f16, odd K
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", ["experts_1024", "experts_1025", "crowded_expert", "f16_x", "k96"])
+def test_grouped_edge_cases(Q, orc, case):
+    rng = np.random.default_rng(sum(map(ord, case)))
+    kind, M, K, E, T = "Q4_0", 64, 256, 16, 6
+    xdt = "f32"
+    if case == "experts_1024":
+        E = 1024
+    elif case == "experts_1025":
+        E = 1025
+    elif case == "f16_x":
+        xdt = "f16"
+    elif case == "k96":
+        K = 96
+    rb = synth.row_bytes(kind, K)
+    w = synth.quant_weights(kind, E * M, K, 71)
+    x = synth.activations(T, K, 72, xdt)
+    n = 24
+    x_row = rng.integers(0, T, n).astype(np.int32)
+    eid = rng.integers(0, E, n).astype(np.int32)
+    if case == "crowded_expert":
+        eid[:11] = 3                      # eleven assignments of one expert, some repeated rows
+        x_row[:11] = np.array([0, 1, 1, 2, 5, 5, 5, 4, 3, 0, 2], dtype=np.int32)
+    Y = sentinel((n, M))
+    Q.qgemm_grouped(kind, dev(w), M * rb, E, dev(x), dev(x_row), dev(eid), M, K, Y=Y)
+    streaming = case in ("experts_1024", "crowded_expert", "f16_x")
+    assert Q.last_path() == (Q.PATH_GROUPED if streaming else Q.PATH_GENERIC)
+    assert Q.check_device_error() == 0
+    y, tol = orc.grouped(kind, w, M * rb, E, x, x_row, eid, M, K)
+    assert_within(Y.cpu().numpy(), y, tol, f"grouped {case}")
