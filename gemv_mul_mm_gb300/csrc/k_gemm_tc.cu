@@ -26,12 +26,20 @@
 // The K-quant mins (-dmin * sum_s m_s * sum_{k in s} x_k) come out of a second,
 // K = 16 (or 32) MMA per super-block: A = the integer mins, B = the per-group
 // activation sums split hi + lo in f16 (a pre-pass kernel), into accumulator D2.
+// Tile schedule: when the 128 x 128 tiles fill the SMs in whole waves, each
+// CTA owns one tile. Otherwise (fewer tiles than SMs, or a ragged last wave)
+// one CTA per SM takes an equal share of the flattened (tile, super-step)
+// sequence: a CTA may end one tile's K range and begin the next one's; whole
+// tiles go straight to Y, parts to a partial-tile workspace that a second
+// kernel (k_tile_fixup) adds up in CTA order -- deterministic, and no CTA
+// ever waits for another.
 // Every wait is bounded (about a second); a timeout latches DEV_ERR_TIMEOUT and
 // the CTA unwinds.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "decode.cuh"
@@ -102,8 +110,86 @@ template <int KIND> struct Mins {
 
 struct TcArgs {
     int M, N, K, nsup;
+    int tiles_m;      // tiles along M; tile t is (t % tiles_m, t / tiles_m)
+    int wq, wr;       // shared super-steps: work = tiles * nsup = wq * G + wr (work < 2^31)
     float* Y;
+    float* part;      // shared tiles: [CTA][2][BN][BM] fp32 partial tiles, or null (one tile per CTA)
     unsigned* err;
+};
+
+// The CTA's share of the flattened (tile, super-step) sequence. Without a
+// partial-tile workspace the grid is (tiles_m, tiles_n) and each CTA takes
+// its own tile's super-steps; with one, the grid is one-dimensional and CTA b
+// takes steps [b * work / G, (b + 1) * work / G), so that every SM gets the
+// same number of super-steps whatever the tile count (a tile's steps may be
+// shared by consecutive CTAs, whose partial sums a second kernel adds up).
+// 32-bit arithmetic only: a 64-bit division is a subroutine call whose
+// register saves spill in this kernel.
+struct Span {
+    int t0, s0, n;    // first tile (-1: the CTA's own tile), its first super-step, steps
+};
+__device__ __forceinline__ Span cta_span(const TcArgs& a) {
+    if (!a.part) return {-1, 0, a.nsup};
+    const int b = blockIdx.x, G = gridDim.x;
+    const int lo = b * a.wq + (b * a.wr) / G;               // floor(b * work / G)
+    const int hi = (b + 1) * a.wq + ((b + 1) * a.wr) / G;
+    return {lo / a.nsup, lo % a.nsup, hi - lo};
+}
+
+// The end of the CTA's part of tile t: a whole tile goes to Y (token-major,
+// ragged edges clipped), a part to the CTA's partial slot -- 0 for the tile
+// it began in, 1 for the tile it ends in. The epilogue thread holds row r,
+// columns half * 64 + [0, 64).
+__device__ __forceinline__ void store_tile(const TcArgs& a, const Span& sp, int t, bool whole, int half, int r,
+                                           const float2 (&acc)[32]) {
+    float* dst;
+    int64_t stride;
+    int lim;
+    if (whole) {
+        const int m0 = sp.t0 < 0 ? static_cast<int>(blockIdx.x) * BM : (t % a.tiles_m) * BM;
+        const int n0 = (sp.t0 < 0 ? static_cast<int>(blockIdx.y) : t / a.tiles_m) * BN + half * 64;
+        const int m = m0 + r;
+        lim = m < a.M ? min(64, a.N - n0) : 0;
+        dst = a.Y + static_cast<int64_t>(n0) * a.M + m;
+        stride = a.M;
+    } else {
+        const int slot = (t == sp.t0) ? 0 : 1;
+        dst = a.part + (static_cast<int64_t>(blockIdx.x * 2 + slot) * BN + half * 64) * BM + r;
+        stride = BM;
+        lim = 64;
+    }
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+        if (i < lim) dst[i * stride] = (i & 1) ? acc[i >> 1].y : acc[i >> 1].x;
+}
+
+// Walks the CTA's steps in order: tile t (rows m0.., tokens n0..) and the
+// super-step s within the tile's K (divisions only when the tile changes).
+struct Step {
+    int t, s, m0, n0;
+    __device__ __forceinline__ Step(const TcArgs& a, const Span& sp) {
+        if (sp.t0 < 0) {
+            t = 0;
+            s = 0;
+            m0 = blockIdx.x * BM;
+            n0 = blockIdx.y * BN;
+        } else {
+            t = sp.t0;
+            s = sp.s0;
+            corner(a);
+        }
+    }
+    __device__ __forceinline__ void corner(const TcArgs& a) {
+        m0 = (t % a.tiles_m) * BM;
+        n0 = (t / a.tiles_m) * BN;
+    }
+    __device__ __forceinline__ void next(const TcArgs& a) {
+        if (++s == a.nsup) {
+            s = 0;
+            ++t;
+            corner(a);
+        }
+    }
 };
 
 // ------------------------------------------------------------ device helpers
@@ -318,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int nsup = a.nsup;
+    // the partial-tile fix-up that follows may be scheduled now; it waits for
+    // this grid to finish before reading anything
+    asm volatile("griddepcontrol.launch_dependents;" :::);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
@@ -361,15 +448,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // each role works out the CTA's span itself (kept out of the registers
+    // live across the roles)
     if (warp == kProdWarp) {
         // ------------------------------------------------ TMA producer: weights (+ group sums)
         if (lane == 0) {
+            const Span span = cta_span(a);
+            const int nloc = span.n;
             int s_issued = 0;
-            for (int s = 0; s < nsup; ++s) {
+            Step st(a, span);
+            for (int s = 0; s < nloc; ++s, st.next(a)) {
                 const int rs = s % RS;
                 if (s >= RS && !wait_bar(&raw_empty[rs], ((s / RS) - 1) & 1, abort_flag, a.err)) break;
                 mbar_arrive_expect_tx(&raw_full[rs], R::STAGE);
-                tma2d(raw + rs * R::STAGE, &tmW, ((s * R::SBB) & ~15) / 2, m0, &raw_full[rs]);
+                tma2d(raw + rs * R::STAGE, &tmW, ((st.s * R::SBB) & ~15) / 2, st.m0, &raw_full[rs]);
                 if constexpr (MN::ON) {
                     const int b = s & 1;
                     if (s >= 2 && !wait_bar(&bmin_empty[b], ((s >> 1) - 1) & 1, abort_flag, a.err)) {
@@ -379,7 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&bmin_full[b], L::MINB);
 #pragma unroll
                     for (int t = 0; t < MN::TILES; ++t)
-                        tma2d(bmin + b * L::MINB + t * MIN_TILE, &tmB, s * MN::KMW + 16 * t, n0, &bmin_full[b]);
+                        tma2d(bmin + b * L::MINB + t * MIN_TILE, &tmB, st.s * MN::KMW + 16 * t, st.n0,
+                              &bmin_full[b]);
                 }
                 s_issued = s + 1;
             }
@@ -393,14 +486,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kXWarp) {
         // ------------------------------------------------ TMA producer: activation sub-tiles
         if (lane == 0) {
+            const Span span = cta_span(a);
+            const int nloc = span.n;
             int sx = 0;
-            const int nx = nsup * (KSUP / KSUB) / 2;   // stages of two sub-steps
+            constexpr int XPS = KSUP / KSUB / 2;         // stages of two sub-steps per super-step
+            const int nx = nloc * XPS;
+            Step st(a, span);
             for (; sx < nx; ++sx) {
+                if (sx > 0 && sx % XPS == 0) st.next(a);
+                const int k0 = (st.s * XPS + sx % XPS) * 2 * KSUB;
                 const int xs = sx % XS;
                 if (sx >= XS && !wait_bar(&x_empty[xs], ((sx / XS) - 1) & 1, abort_flag, a.err)) break;
                 mbar_arrive_expect_tx(&x_full[xs], X_TILE);
-                tma2d(x_tiles + xs * X_TILE, &tmX, 2 * sx * KSUB, n0, &x_full[xs]);
-                tma2d(x_tiles + xs * X_TILE + X_SUB, &tmX, (2 * sx + 1) * KSUB, n0, &x_full[xs]);
+                tma2d(x_tiles + xs * X_TILE, &tmX, k0, st.n0, &x_full[xs]);
+                tma2d(x_tiles + xs * X_TILE + X_SUB, &tmX, k0 + KSUB, st.n0, &x_full[xs]);
             }
             for (int i = (sx > XS ? sx - XS : 0); i < sx; ++i) drain_bar(&x_full[i % XS], (i / XS) & 1, a.err);
         }
@@ -411,8 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // behind MMAs stalls for ~100 cycles): the waits are done by the
         // waiter warp, which hands each ready sub-step over through a named
         // barrier (bar.red also carries whether to go on).
+        const int nloc = cta_span(a).n;
         int sub = 0;
-        for (int s = 0; s < nsup; ++s) {
+        for (int s = 0; s < nloc; ++s) {
             for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
                 const bool go = bar_red_and(kBarHand + (sub & 1), 64, true);
                 if (go && lane == 0) {
@@ -465,9 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stage, its activation stage, free accumulators and, at the end of a
         // super-block, the mins tiles -- then releases it to the issuer. After
         // a failure it keeps handing over "stop" so both sides stay in step.
+        const int nloc = cta_span(a).n;
         int sub = 0;
         bool ok = true;
-        for (int s = 0; s < nsup; ++s) {
+        for (int s = 0; s < nloc; ++s) {
             for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
                 if (lane == 0 && ok) {
                     const int as = sub % AS, xi = sub >> 1, xs = xi % XS;
@@ -500,11 +601,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // weight row within the tile = the TMEM lane this warp may access
         const int r = (warp & 3) * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const Span span = cta_span(a);
+        const int nloc = span.n;
         int sub = 0;
-        for (int s = 0; s < nsup; ++s) {
+        int ks = span.s0;   // super-step within the row
+        for (int s = 0; s < nloc; ++s, ks = (ks + 1 == a.nsup) ? 0 : ks + 1) {
             const int rs = s % RS;
             bool ok = warp_wait_bar(&raw_full[rs], (s / RS) & 1, abort_flag, a.err);
-            const uint8_t* row = raw + rs * R::STAGE + r * R::BOXB + ((s * R::SBB) & 15);
+            const uint8_t* row = raw + rs * R::STAGE + r * R::BOXB + ((ks * R::SBB) & 15);
             // scales for the epilogue
             if (ok && s >= 2) ok = warp_wait_bar(&sc_empty[s & 1], ((s >> 1) - 1) & 1, abort_flag, a.err);
             float* sc = sbuf + ((s & 1) * BM + r) * 8;
@@ -593,74 +697,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 acc[32];   // columns 2i, 2i + 1 of this thread's 64, updated with packed FMAs
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
-        for (int s = 0; s < nsup; ++s) {
-            const float* sc = sbuf + ((s & 1) * BM + r) * 8;
-            warp_wait_bar(&sc_full[s & 1], (s >> 1) & 1, abort_flag, a.err);
-            if constexpr (PER32) {
-                for (int j = 0; j < 8; ++j) {
-                    const int u = 8 * s + j, b = u % ND;
-                    const bool ok = warp_wait_bar(&d_full[b], (u / ND) & 1, abort_flag, a.err);
+        const Span span = cta_span(a);
+        const int nloc = span.n;
+        // one segment per tile the CTA works on; the tile is stored after
+        // its last super-step (the store sits outside the per-step loop: the
+        // accumulators stay in registers)
+        int et = span.t0, es = span.s0;   // the segment's tile and first super-step
+        for (int s = 0; s < nloc;) {
+            const int seg_end = min(nloc, s + a.nsup - es);
+            const bool whole = es == 0 && seg_end - s == a.nsup;
+            for (; s < seg_end; ++s) {
+                const float* sc = sbuf + ((s & 1) * BM + r) * 8;
+                warp_wait_bar(&sc_full[s & 1], (s >> 1) & 1, abort_flag, a.err);
+                if constexpr (PER32) {
+                    for (int j = 0; j < 8; ++j) {
+                        const int u = 8 * s + j, b = u % ND;
+                        const bool ok = warp_wait_bar(&d_full[b], (u / ND) & 1, abort_flag, a.err);
+                        tc_fence_after();
+                        const float2 d2 = make_float2(sc[j], sc[j]);
+                        if (ok) {
+#pragma unroll
+                            for (int c = 0; c < 4; c += 2) {
+                                float v[32];
+                                tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16,
+                                          *reinterpret_cast<float(*)[16]>(v));
+                                tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16 + 16,
+                                          *reinterpret_cast<float(*)[16]>(v + 16));
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    acc[c * 8 + i] = __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]), acc[c * 8 + i]);
+                            }
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&d_empty[b]);
+                    }
+                } else {
+                    const int b = s & 1;
+                    const bool ok = warp_wait_bar(&d_full[b], (s >> 1) & 1, abort_flag, a.err);
                     tc_fence_after();
-                    const float2 d2 = make_float2(sc[j], sc[j]);
+                    const float2 d2 = make_float2(sc[0], sc[0]), ndm2 = make_float2(-sc[1], -sc[1]);
                     if (ok) {
 #pragma unroll
-                        for (int c = 0; c < 4; c += 2) {
-                            float v[32];
-                            tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16,
-                                      *reinterpret_cast<float(*)[16]>(v));
-                            tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16 + 16,
-                                      *reinterpret_cast<float(*)[16]>(v + 16));
-                            tmem_wait_ld();
+                        for (int c = 0; c < 4; ++c) {
+                            float v[16];
+                            tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16, v);
+                            if constexpr (MN::ON) {
+                                float w2[16];
+                                tmem_ld16(tmem + lane_addr + kDCol0 + 2 * BN + half * 64 + c * 16, w2);
+                                tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                acc[c * 8 + i] = __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]), acc[c * 8 + i]);
+                                for (int i = 0; i < 8; ++i)
+                                    acc[c * 8 + i] = __ffma2_rn(ndm2, make_float2(w2[2 * i], w2[2 * i + 1]),
+                                                                __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]),
+                                                                           acc[c * 8 + i]));
+                            } else {
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    acc[c * 8 + i] = __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]), acc[c * 8 + i]);
+                            }
                         }
                     }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&d_empty[b]);
                 }
-            } else {
-                const int b = s & 1;
-                const bool ok = warp_wait_bar(&d_full[b], (s >> 1) & 1, abort_flag, a.err);
-                tc_fence_after();
-                const float2 d2 = make_float2(sc[0], sc[0]), ndm2 = make_float2(-sc[1], -sc[1]);
-                if (ok) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float v[16];
-                        tmem_ld16(tmem + lane_addr + kDCol0 + b * BN + half * 64 + c * 16, v);
-                        if constexpr (MN::ON) {
-                            float w2[16];
-                            tmem_ld16(tmem + lane_addr + kDCol0 + 2 * BN + half * 64 + c * 16, w2);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                acc[c * 8 + i] = __ffma2_rn(ndm2, make_float2(w2[2 * i], w2[2 * i + 1]),
-                                                            __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]),
-                                                                       acc[c * 8 + i]));
-                        } else {
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                acc[c * 8 + i] = __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]), acc[c * 8 + i]);
-                        }
-                    }
-                }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&d_empty[b]);
+                if (lane == 0) mbar_arrive(&sc_empty[s & 1]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sc_empty[s & 1]);
-        }
-        const int m = m0 + r;
-        if (m < a.M && !*abort_flag) {
+            if (!*abort_flag) store_tile(a, span, et, whole, half, r, acc);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const int n = n0 + half * 64 + i;
-                if (n < a.N) a.Y[static_cast<int64_t>(n) * a.M + m] = (i & 1) ? acc[i >> 1].y : acc[i >> 1].x;
-            }
+            for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
+            es = 0;
+            ++et;
         }
     }
 
@@ -710,6 +821,45 @@ __global__ void k_xsums(const __half* __restrict__ X, int N, int K, int gsize, i
     }
 }
 
+// Adds up the partial tiles of the tiles whose super-steps were shared by
+// several CTAs, in CTA order, and writes them to Y (the CTA that covers a
+// whole tile has already written it). Grid (tiles, kFixSplit): each thread
+// takes four consecutive rows of one token of the tile, a float4 of every
+// partial that covers it.
+constexpr int kFixThreads = 256;
+constexpr int kFixSplit = BM * BN / 4 / kFixThreads;
+__global__ void __launch_bounds__(kFixThreads) k_tile_fixup(const float* __restrict__ part, float* __restrict__ Y,
+                                                            int M, int N, int tiles_m, int nsup, int64_t work,
+                                                            int G) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int t = blockIdx.x;
+    // CTA b covers steps [b * work / G, (b + 1) * work / G): step g lies in CTA ((g + 1) * G - 1) / work
+    const int64_t g0 = static_cast<int64_t>(t) * nsup, g1 = g0 + nsup - 1;
+    const int b0 = static_cast<int>(((g0 + 1) * G - 1) / work), b1 = static_cast<int>(((g1 + 1) * G - 1) / work);
+    if (b0 == b1) return;
+    // the first CTA holds the tile in slot 0 if it began at the tile's first
+    // step, else in slot 1 (its last tile); every later one began inside it
+    const int slot0 = (static_cast<int64_t>(b0) * work / G == g0) ? 0 : 1;
+    const int q = blockIdx.y * kFixThreads + threadIdx.x;   // float4 index within the tile
+    const int nl = q / (BM / 4), ml = (q % (BM / 4)) * 4;
+    const int m0 = (t % tiles_m) * BM + ml, n = (t / tiles_m) * BN + nl;
+    if (n >= N || m0 >= M) return;
+    const float4* p4 = reinterpret_cast<const float4*>(part) + q;
+    float4 v = p4[(static_cast<int64_t>(b0) * 2 + slot0) * (BM * BN / 4)];
+    for (int b = b0 + 1; b <= b1; ++b) {
+        const float4 u = p4[static_cast<int64_t>(b) * 2 * (BM * BN / 4)];
+        v.x += u.x;
+        v.y += u.y;
+        v.z += u.z;
+        v.w += u.w;
+    }
+    float* y = Y + static_cast<int64_t>(n) * M + m0;
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (m0 + i < M) y[i] = vv[i];
+}
+
 // ------------------------------------------------------------ host side
 bool make_map(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
               uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
@@ -757,6 +907,32 @@ void ok_kind(const Problem& p, bool* out) {
            p.M <= (int64_t(1) << 30) && p.N <= (int64_t(1) << 30) && p.K <= (int64_t(1) << 30);
 }
 
+// QMM_TC_SPLIT: 0 = automatic, 1 = one tile per CTA always, 2 = shared
+// super-steps whenever possible (for measurements).
+const int kEnvSplit = [] {
+    const char* v = getenv("QMM_TC_SPLIT");
+    return v ? atoi(v) : 0;
+}();
+// Estimated cost, in super-steps, of sharing tiles: the partial-tile stores
+// and the fix-up kernel. Measured on 4096 x 4096 x 512 (128 tiles, 16 steps
+// each): sharing (14 steps per CTA) ran 8 % slower than one tile per CTA, so
+// the fix-up costs about 3 of that workload's super-steps; 11008 x 4096 x 128
+// (86 tiles) ran 22 - 28 % faster shared (10 steps per CTA instead of 16).
+constexpr int kSplitCost = 3;
+
+// Grid size when the CTAs share the tiles' super-steps, or 0 for one CTA per
+// tile. One tile per CTA takes ceil(tiles / SMs) waves of nsup super-steps;
+// sharing takes ceil(tiles * nsup / SMs) super-steps per CTA plus the fix-up.
+int split_grid(int64_t tiles, int nsup, int sms) {
+    const int64_t work = tiles * nsup;
+    if (kEnvSplit == 1 || sms <= 0 || work >= (int64_t(1) << 31)) return 0;
+    const int G = static_cast<int>(imin64(sms, work));
+    if (kEnvSplit == 2) return G;
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const int64_t per = (work + G - 1) / G;
+    return (per + kSplitCost < waves * nsup) ? G : 0;
+}
+
 template <int KIND>
 void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     using R = Raw<KIND>;
@@ -764,6 +940,23 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     using L = Layout<KIND>;
     const int M = static_cast<int>(p.M), N = static_cast<int>(p.N), K = static_cast<int>(p.K);
     const int nsup = K / KSUP;
+    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
+    int dev = 0;
+    if ((*e = cudaGetDevice(&dev)) != cudaSuccess) return;
+    const int G = split_grid(tiles, nsup, sm_count(dev));
+    // one workspace: the activation sums (formats with mins), then the partial tiles
+    const size_t xs_bytes = MN::ON ? ((static_cast<size_t>(N) * nsup * MN::KMW * 2 + 255) & ~size_t(255)) : 0;
+    const size_t part_bytes = static_cast<size_t>(G) * 2 * BM * BN * sizeof(float);
+    uint8_t* ws = nullptr;
+    if (xs_bytes + part_bytes) {
+        bool capturing = false;
+        ws = static_cast<uint8_t*>(workspace(xs_bytes + part_bytes, s, &capturing));
+        if (!ws) {
+            *e = capturing ? cudaErrorStreamCaptureUnsupported : cudaErrorMemoryAllocation;
+            return;
+        }
+    }
     CUtensorMap tmW, tmX, tmB;
     if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, p.row_bytes / 2, M, p.row_bytes, R::BOXB / 2, BM,
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -774,18 +967,11 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     }
     tmB = tmX;
     if constexpr (MN::ON) {
-        const size_t ws_bytes = static_cast<size_t>(N) * nsup * MN::KMW * 2;
-        bool capturing = false;
-        void* ws = workspace(ws_bytes, s, &capturing);
-        if (!ws) {
-            *e = capturing ? cudaErrorStreamCaptureUnsupported : cudaErrorMemoryAllocation;
-            return;
-        }
         const int threads = 256;
         const int64_t total = static_cast<int64_t>(N) * (K / (KSUP / MN::G));
         const int blocks = static_cast<int>(imin64((total + threads - 1) / threads, 4096));
         k_xsums<<<blocks, threads, 0, s>>>(static_cast<const __half*>(p.X), N, K, KSUP / MN::G, MN::G,
-                                           static_cast<__half*>(ws));
+                                           reinterpret_cast<__half*>(ws));
         count_launch(1);
         if ((*e = cudaGetLastError()) != cudaSuccess) return;
         if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws, static_cast<uint64_t>(nsup) * MN::KMW, N,
@@ -801,12 +987,29 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     a.N = N;
     a.K = K;
     a.nsup = nsup;
+    a.tiles_m = tiles_m;
+    a.wq = G ? static_cast<int>(tiles * nsup / G) : 0;
+    a.wr = G ? static_cast<int>(tiles * nsup % G) : 0;
     a.Y = p.Y;
+    a.part = G ? reinterpret_cast<float*>(ws + xs_bytes) : nullptr;
     a.err = p.err;
-    const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);
+    const dim3 grid = G ? dim3(G) : dim3(tiles_m, tiles_n);
     kern<<<grid, kThreads, L::BYTES, s>>>(tmW, tmX, tmB, a);
     count_launch(1);
-    *e = cudaGetLastError();
+    if ((*e = cudaGetLastError()) != cudaSuccess || !G) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles), kFixSplit);
+    cfg.blockDim = dim3(kFixThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    *e = cudaLaunchKernelEx(&cfg, k_tile_fixup, static_cast<const float*>(a.part), a.Y, M, N, tiles_m, nsup,
+                            tiles * nsup, G);
+    count_launch(1);
+    if (*e == cudaSuccess) *e = cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -893,7 +1096,11 @@ void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
     a.N = N;
     a.K = K;
     a.nsup = nsup;
+    a.tiles_m = (M + BM - 1) / BM;
+    a.wq = 0;
+    a.wr = 0;
     a.Y = p.Y;
+    a.part = nullptr;   // one tile per CTA: no partial-tile scratch
     a.err = p.err;
     const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);
     kern<<<grid, kThreads, L::BYTES, s>>>(tmW, tmX, tmB, a);

@@ -153,12 +153,16 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
  *
  * Accuracy: |Y - Y_exact| <= 1e-3 * sum_k |W[m,k] * X[n,k]| + 1e-6 per element.
  *
- * Workspace: the tensor-core path for Q4_K, Q5_K and Q2_K stores per-group
- * activation sums (N * K/16 f16 values at most) in a per-device workspace the
- * library owns and grows on demand (cudaMalloc). Growth is refused during
- * stream capture (QMM_ERR_WORKSPACE_IN_CAPTURE): make one call of the largest
- * shape before capturing. Concurrent calls on different streams of one device
- * share that workspace and must not overlap.
+ * Workspace: the tensor-core path keeps two things in a per-device workspace
+ * the library owns and grows on demand (cudaMalloc): for Q4_K, Q5_K and Q2_K
+ * the per-group activation sums (N * K/16 f16 values at most), and, when the
+ * 128 x 128 output tiles do not fill the GPU evenly, the partial tiles of
+ * the tiles whose K range several CTAs share (2 * 64 KiB per SM). Those
+ * partial sums are added in a fixed order by a second kernel, so results are
+ * deterministic. Growth is refused during stream capture
+ * (QMM_ERR_WORKSPACE_IN_CAPTURE): make one call of the largest shape before
+ * capturing. Concurrent calls on different streams of one device share that
+ * workspace and must not overlap.
  */
 QMM_API int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
           float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream);
@@ -171,8 +175,10 @@ QMM_API int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_
  * the capture), and runtimes that reserve all device memory up front and
  * hand out only their own pools.
  *
- * It computes exactly what qgemm computes, with the same arguments, layouts
- * and accuracy, but only on the tensor-core path: f16 activations, K a
+ * It computes what qgemm computes, with the same arguments, layouts and
+ * accuracy (one CTA per output tile, never shared K ranges, so the rounding
+ * of the sums can differ from qgemm's), but only on the tensor-core path:
+ * f16 activations, K a
  * multiple of 256, 16-byte aligned W and X, rows a multiple of 16 bytes
  * (QMM_ERR_UNIMPLEMENTED otherwise). The per-group activation sums that
  * Q4_K, Q5_K and Q2_K need go to a fixed 4 MiB device array compiled into the

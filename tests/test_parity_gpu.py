@@ -219,6 +219,43 @@ def test_prefill_gemm_sampled(Q, orc, cfg, kind):
     assert_within(got[n, m], y, tol, f"{kind} prefill (path {Q.last_path()})")
 
 
+# Tile schedules of the tensor-core GEMM. When the 128 x 128 output tiles do
+# not fill the SMs evenly, consecutive CTAs share a tile's K range and a second
+# kernel adds their partial tiles; otherwise each CTA owns one tile.
+#   many_partials: 6 tiles (ragged in M and N), 32 super-steps each, on every
+#                  SM -- each tile's sum is split over about 25 CTAs;
+#   whole_inside:  190 tiles (ragged in M) of 8 super-steps over the SMs --
+#                  CTAs take one or two partial tiles and whole tiles between;
+#   one_per_cta:   152 tiles of one super-step -- one wave, no sharing.
+SCHEDULES = {"many_partials": (300, 8192, 150), "whole_inside": (24300, 2048, 128),
+             "one_per_cta": (19456, 256, 128)}
+
+
+@pytest.mark.parametrize("case,kind", [("many_partials", "Q4_K"), ("many_partials", "IQ4_NL"),
+                                       ("many_partials", "Q6_K"), ("whole_inside", "Q4_K"),
+                                       ("whole_inside", "MXFP4"), ("one_per_cta", "Q5_K"),
+                                       ("one_per_cta", "IQ4_NL")])
+def test_gemm_tile_schedules(Q, orc, case, kind):
+    M, K, N = SCHEDULES[case]
+    seed = sum(map(ord, case + kind))
+    w = synth.quant_weights(kind, M, K, seed)
+    x = synth.activations(N, K, seed + 1, "f16")
+    Y = sentinel((N, M))
+    Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
+    assert Q.last_path() == Q.PATH_TC
+    assert Q.check_device_error() == 0
+    got = Y.cpu().numpy()
+    assert not np.any(got == SENTINEL)
+    # whole token columns (every tile along M) and whole weight rows (every
+    # tile along N): first, middle and last of each
+    cols = np.array([0, N // 2 + 1, N - 1]) if case != "whole_inside" else np.array([0, N - 1])
+    rows = np.array([0, M // 2, M - 1])
+    n = np.concatenate([np.repeat(cols, M), np.tile(np.arange(N), rows.size)])
+    m = np.concatenate([np.tile(np.arange(M), cols.size), np.repeat(rows, N)])
+    y, tol = orc.gemm_at(kind, w, M, K, x, n, m)
+    assert_within(got[n, m], y, tol, f"{kind} {case}")
+
+
 @pytest.mark.parametrize("T", synth.MOE["tokens"])
 @pytest.mark.parametrize("which", ["gate_up", "down"])
 def test_moe_grouped(Q, orc, T, which):
