@@ -1,0 +1,41 @@
+"""Host-side logic of bench.py that needs no GPU.
+
+The roofline's `traffic` figure comes from DRAM counters committed under
+profiles/, valid only while the kernel they were taken on is unchanged: the
+check hashes the kernel sources with their comments stripped, so a comment
+edit keeps the counters and any code edit drops them.
+"""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_strip_comments_keeps_code_and_literals():
+    src = ('int a = 1; // note\n'
+           '/* block\n   comment */ int b = 2;\n'
+           'const char* s = "// not a comment";\n'
+           "char c = '/';\n"
+           '\n'
+           'asm volatile("bar.sync %0, %1;" ::"r"(x));  /* trailing */\n')
+    out = bench.strip_comments(src)
+    assert out.splitlines() == ['int a = 1;', ' int b = 2;', 'const char* s = "// not a comment";',
+                                "char c = '/';", 'asm volatile("bar.sync %0, %1;" ::"r"(x));']
+
+
+def test_comment_edit_keeps_hash_code_edit_changes_it():
+    base = "__global__ void k(float* y) {\n    y[0] = 1.f;  // store\n}\n"
+    reworded = "// a kernel\n__global__ void k(float* y) {\n    y[0] = 1.f;  /* the store */\n}\n"
+    changed = "__global__ void k(float* y) {\n    y[1] = 1.f;  // store\n}\n"
+    s = bench.strip_comments
+    assert s(base) == s(reworded)
+    assert s(base) != s(changed)
+
+
+def test_committed_traffic_matches_current_gemv_sources():
+    # the committed DRAM counters were taken on the kernel as it is now
+    assert bench.traffic_for("k_gemv<Q8_0>", ["k_gemv.cu", "decode.cuh", "sm100_async.cuh"]) == 62510336
+    assert bench.traffic_for("k_gemv<Q4_0>", ["k_gemv.cu", "decode.cuh", "sm100_async.cuh"]) == 33130240
