@@ -256,6 +256,65 @@ def test_gemm_tile_schedules(Q, orc, case, kind):
     assert_within(got[n, m], y, tol, f"{kind} {case}")
 
 
+def test_gemm_graph_replay_is_bit_identical_to_eager(Q, orc):
+    # 16 tiles of 16 super-steps: the K ranges are shared over all SMs and
+    # the partial tiles are added in a fixed order, so a replayed graph gives
+    # the eager call's bits exactly
+    import torch
+    kind, (M, K, N) = "IQ4_NL", (1000, 4096, 130)
+    w = synth.quant_weights(kind, M, K, 91)
+    x = synth.activations(N, K, 92, "f16")
+    Wd, Xd = dev(w), dev(x)
+    Ye = Q.qgemm(kind, Wd, Xd, M, K, N)          # eager: the workspace grows here
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    Yg = sentinel((N, M))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        Q.qgemm(kind, Wd, Xd, M, K, N, Y=Yg, stream=s.cuda_stream)
+    for _ in range(2):
+        Yg.fill_(SENTINEL)
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(Ye, Yg)
+    assert Q.check_device_error() == 0
+    n, m = sample_positions(N, M, 300, 93)
+    y, tol = orc.gemm_at(kind, w, M, K, x, n, m)
+    assert_within(Ye.cpu().numpy()[n, m], y, tol, "eager")
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
+def test_workspace_growth_during_capture_is_refused(Q, orc):
+    # activation sums of 16384 tokens x 64 super-blocks (33.5 MB) plus the
+    # partial tiles: more workspace than any other test needs, so the
+    # library must grow it -- which it refuses inside a capture, before
+    # launching anything; the capture ends cleanly and the next eager call
+    # grows the workspace and computes
+    import torch
+    kind, (M, K, N) = "Q4_K", (256, 16384, 16384)
+    w = synth.quant_weights(kind, M, K, 95)
+    Wd = dev(w)
+    Xd = torch.empty((N, K), dtype=torch.float16, device="cuda")
+    Y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(Q.QmmError) as ei:
+        with torch.cuda.graph(g, stream=s):
+            Q.qgemm(kind, Wd, Xd, M, K, N, Y=Y, stream=s.cuda_stream)
+    assert ei.value.name == "QMM_ERR_WORKSPACE_IN_CAPTURE"
+    torch.cuda.synchronize()
+    x = synth.activations(64, K, 96, "f16")
+    Xd[:64].copy_(dev(x).view(64, K))
+    Q.qgemm(kind, Wd, Xd, M, K, N, Y=Y)
+    torch.cuda.synchronize()
+    assert Q.check_device_error() == 0
+    n, m = sample_positions(64, M, 200, 97)
+    y, tol = orc.gemm_at(kind, w, M, K, x, n, m)
+    assert_within(Y.cpu().numpy()[n, m], y, tol, "after the refused capture")
+
+
 @pytest.mark.parametrize("T", synth.MOE["tokens"])
 @pytest.mark.parametrize("which", ["gate_up", "down"])
 def test_moe_grouped(Q, orc, T, which):
