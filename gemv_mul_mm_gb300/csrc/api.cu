@@ -171,6 +171,8 @@ int qmm_set_weight_prefetch(int on) { return g_prefetch.exchange(on ? 1 : 0); }
 
 uint64_t qmm_launch_count(void) { return g_launches.load(); }
 
+int qmm_shutdown(void) { return qmm::release_gemm_workspaces() ? QMM_OK : QMM_ERR_CUDA; }
+
 int qdequant(int kind, const void* blocks, size_t blocks_bytes, int64_t rows, int64_t cols,
              float* out, size_t out_elems, void* stream) {
     if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;

@@ -900,6 +900,22 @@ void* workspace(size_t bytes, cudaStream_t s, bool* capturing) {
     return w.ptr;
 }
 
+bool release_workspaces() {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return false;
+    bool ok = true;
+    for (int dev = 0; dev < 64; ++dev) {
+        Workspace& w = g_ws[dev];
+        if (!w.ptr) continue;
+        if (cudaSetDevice(dev) != cudaSuccess || cudaFree(w.ptr) != cudaSuccess) ok = false;
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    if (cudaSetDevice(cur) != cudaSuccess) ok = false;
+    return ok;
+}
+
 template <int KIND>
 void ok_kind(const Problem& p, bool* out) {
     *out = !p.x_row && p.x_dtype == 1 && p.K % KSUP == 0 && p.row_bytes % 16 == 0 &&
@@ -1109,6 +1125,8 @@ void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
 }
 
 }  // namespace
+
+bool release_gemm_workspaces() { return release_workspaces(); }
 
 int launch_gemm_tc_noalloc(const Problem& p, cudaStream_t s) {
     int status = 0;

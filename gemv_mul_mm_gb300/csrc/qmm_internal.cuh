@@ -71,5 +71,7 @@ cudaError_t launch_gemm_tc(const Problem& p, cudaStream_t s);
 // Same GEMM with its scratch in a fixed device array (no allocation);
 // returns a qmm_status code.
 int launch_gemm_tc_noalloc(const Problem& p, cudaStream_t s);
+// Frees the GEMM's grown workspaces on every device; false if a free failed.
+bool release_gemm_workspaces();
 
 }  // namespace qmm

@@ -69,6 +69,7 @@ def _lib():
         L.qmm_set_path.argtypes = [_I]
         L.qmm_set_weight_prefetch.argtypes = [_I]
         L.qmm_launch_count.restype = ctypes.c_uint64
+        L.qmm_shutdown.argtypes = []
         _LIB = L
     return _LIB
 
@@ -200,6 +201,11 @@ def qgemm_grouped(kind, W, expert_stride: int, n_experts: int, X, x_row, expert_
 def selftest_wait_timeout(cycles: int, stream=None):
     """Queue the failure-path self-test kernel (a bounded wait that runs out)."""
     _check(_lib().qmm_selftest_wait_timeout(int(cycles), _stream(stream)), "qmm_selftest_wait_timeout")
+
+
+def shutdown():
+    """Free the library's grown per-device workspaces (later calls regrow them)."""
+    _check(_lib().qmm_shutdown(), "qmm_shutdown")
 
 
 def check_device_error(stream=None) -> int:

@@ -268,6 +268,16 @@ QMM_API int qmm_last_path(void);
 /* Number of kernels this library has launched since load (all threads). */
 QMM_API uint64_t qmm_launch_count(void);
 
+/*
+ * qmm_shutdown -- frees the per-device workspaces qgemm grows (activation
+ * sums, partial tiles; see qgemm) on every device that has one. cudaFree
+ * waits for the work in flight on that device first. Later calls grow them
+ * again as needed. Not to be called while another thread is inside the
+ * library. Returns QMM_OK, or QMM_ERR_CUDA if a free failed (the remaining
+ * ones are still attempted). The current device is left as it was.
+ */
+QMM_API int qmm_shutdown(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -315,6 +315,24 @@ def test_workspace_growth_during_capture_is_refused(Q, orc):
     assert_within(Y.cpu().numpy()[n, m], y, tol, "after the refused capture")
 
 
+def test_shutdown_frees_workspaces_and_calls_regrow_them(Q, orc):
+    import torch
+    kind, (M, K, N) = "Q4_K", (300, 4096, 150)     # activation sums + shared tiles
+    w = synth.quant_weights(kind, M, K, 98)
+    x = synth.activations(N, K, 99, "f16")
+    Wd, Xd = dev(w), dev(x)
+    Y1 = Q.qgemm(kind, Wd, Xd, M, K, N)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    Q.shutdown()
+    Q.shutdown()                                    # nothing left to free: still fine
+    assert torch.cuda.mem_get_info()[0] > free0     # the workspace went back to the device
+    Y2 = Q.qgemm(kind, Wd, Xd, M, K, N)              # grows it again
+    torch.cuda.synchronize()
+    assert Q.check_device_error() == 0
+    assert torch.equal(Y1, Y2)
+
+
 @pytest.mark.parametrize("T", synth.MOE["tokens"])
 @pytest.mark.parametrize("which", ["gate_up", "down"])
 def test_moe_grouped(Q, orc, T, which):
