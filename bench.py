@@ -330,6 +330,21 @@ def secondary_table(qmm, synth, l2_bytes, stream, pk):
     ms = bench_fn(lambda i: qmm.qgemm("Q4_0", w, x, c["M"], c["K"], c["N"], Y=y, stream=stream.cuda_stream), 1)
     out["tiny_q4_0_qgemm"] = {"us": round(ms * 1e3, 3), "path": qmm.last_path(),
                               "tflops": round(2 * c["M"] * c["K"] * c["N"] / (ms * 1e-3) / 1e12, 4)}
+    deq = {}
+
+    def dequant_row(kind, w, copies, M, K):
+        # bit-exact dequant to fp32: the weight bytes read plus 4 * M * K written
+        try:
+            o = torch.empty((M, K), device="cuda")
+            ms = bench_fn(lambda i: qmm.qdequant(kind, w[i % copies], M, K, out=o, stream=stream.cuda_stream),
+                          copies, reps=max(copies, 5), replays=3)
+            byt = w[0].numel() + 4 * M * K
+            deq[kind] = {"M": M, "K": K, "us": round(ms * 1e3, 2), "gbs": round(byt / (ms * 1e-3) / 1e9, 1),
+                         "frac_of_hbm": round(byt / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+            del o
+        except Exception as e:   # a failure here must not cost the bench line
+            deq[kind] = {"error": f"{type(e).__name__}: {e}"[:200]}
+
     # prefill GEMMs
     gem = {}
     for cfg in (synth.KQUANT, synth.CODEBOOK):
@@ -345,6 +360,7 @@ def secondary_table(qmm, synth, l2_bytes, stream, pk):
             tf = 2 * M * K * N / (ms * 1e-3) / 1e12
             gem[kind] = {"M": M, "K": K, "N": N, "us": round(ms * 1e3, 2), "tflops": round(tf, 2),
                          "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4), "path": qmm.last_path()}
+            dequant_row(kind, ws, copies, M, K)
             del ws
     out["gemm"] = gem
     # MoE grouped: both projections of the layer
@@ -373,6 +389,20 @@ def secondary_table(qmm, synth, l2_bytes, stream, pk):
     byt = wh.numel() + 4 * c["M"] * c["K"]
     out["dequant_q4_0"] = {"us": round(ms * 1e3, 2), "gbs": round(byt / (ms * 1e-3) / 1e9, 1),
                            "frac_of_hbm": round(byt / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+    del wh, o
+    # dequant of every kind on its workload tensor: Q8_0, Q4_0 and Q5_0 on the
+    # decode shape, the K-quants and the codebook kinds on their GEMM shapes
+    # (timed above, beside each GEMM)
+    for kind in ("Q8_0", "Q4_0", "Q5_0"):
+        try:
+            w = [torch.from_numpy(synth.workload_weights(c, kind)).cuda()]
+        except Exception as e:
+            deq[kind] = {"error": f"{type(e).__name__}: {e}"[:200]}
+            continue
+        dequant_row(kind, w, 1, c["M"], c["K"])
+        del w
+    out["dequant"] = {k: deq[k] for k in ("Q8_0", "Q4_0", "Q5_0", "Q4_K", "Q5_K", "Q6_K", "Q2_K", "Q3_K",
+                                          "IQ4_NL", "IQ4_XS", "MXFP4") if k in deq}
     return out
 
 
