@@ -39,3 +39,26 @@ def test_committed_traffic_matches_current_gemv_sources():
     # the committed DRAM counters were taken on the kernel as it is now
     assert bench.traffic_for("k_gemv<Q8_0>", ["k_gemv.cu", "decode.cuh", "sm100_async.cuh"]) == 62510336
     assert bench.traffic_for("k_gemv<Q4_0>", ["k_gemv.cu", "decode.cuh", "sm100_async.cuh"]) == 33130240
+
+
+def test_reference_arm_json_line_keeps_the_contract():
+    # the CPU oracle arm: one JSON line with the keys the bench contract names,
+    # its cpu_baseline and e2e describing this same run
+    import json
+    import subprocess
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] == 0 and d["n_gpus"] == 1
+    assert d["higher_is_better"] is True and d["value"] > 0 and d["unit"] == "GB/s"
+    assert "workload" in d["config"] and "model" not in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
