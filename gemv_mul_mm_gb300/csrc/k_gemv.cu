@@ -43,10 +43,11 @@
 //     packed subtract leaves q. Both multiply with packed fp32x2 FMAs; the fp32
 //     block scale multiplies the block's partial sum.
 //   * Programmatic dependent launch: the kernel lets the next one on the stream
-//     launch at once, and its shared memory is small enough for two CTAs per
-//     SM, so (when the caller declares the weights constant) the next GEMV
-//     streams its first weight stages while this one drains. Activations and
-//     expert ids are read only after `griddepcontrol.wait`.
+//     launch at once. When the caller declares the weights constant, each CTA
+//     of the next GEMV streams its first weight stages as soon as it is
+//     resident -- beside this kernel's CTAs when the stage ring fits two CTAs
+//     per SM, else as this kernel's CTAs retire -- while this one drains.
+//     Activations and expert ids are read only after `griddepcontrol.wait`.
 //
 // The P4 page's v3 lesson (stage x in shared memory, keep lanes on distinct
 // banks, keep loads in flight) is kept; its f16x2 accumulation is not (too
