@@ -525,6 +525,12 @@ def run_ours(a):
         rate, steps, el, wb = oracle_decode_rate(kinds, M, K, 10.0, cores)
         cpu = {"value": round(rate, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{steps} full decode steps ({wb} weight bytes each) in {el:.1f} s"}
+        try:   # the same oracle on one core, for scale
+            r1, s1, e1, _ = oracle_decode_rate(kinds, M, K, 4.0, 1)
+            cpu["single_thread"] = {"value": round(r1, 3), "unit": UNIT, "cores": 1,
+                                    "sample": f"{s1} full decode steps in {e1:.1f} s"}
+        except Exception as e:
+            cpu["single_thread"] = {"error": f"{type(e).__name__}: {e}"[:200]}
 
     sec = None
     if d.rank == 0 and d.world == 1 and not a.no_secondary:
