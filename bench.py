@@ -269,10 +269,10 @@ def src_hash(*names):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel_key: str, srcs):
+def traffic_for(kernel_key: str, srcs, path: str = None):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     kernel source changed since the counters were taken."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    p = path or os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -418,9 +418,6 @@ def run_ours(a):
     from gemv_mul_mm_gb300 import qmm, synth
 
     pk, pk_src = peaks()
-    # model weights are constant while steps are in flight: let each GEMV start
-    # streaming its weights while the previous kernel drains
-    qmm.set_weight_prefetch(True)
     c = synth.DECODE
     kinds, M, K = c["kinds"], c["M"], c["K"]
     props = torch.cuda.get_device_properties(d.local)
@@ -442,7 +439,7 @@ def run_ours(a):
     def one_step(i):
         j = i % copies
         for k in kinds:
-            qmm.qgemv(k, W[k][j], X[k], M, K, y=Y[k], stream=sh)
+            qmm.qgemv(k, W[k][j], X[k], M, K, y=Y[k], stream=sh, weights_const=True)
 
     # Steps are replayed from CUDA graphs of R consecutive steps (rotating the
     # weight copies), plus one graph for the remainder, so exactly K steps run.
@@ -481,7 +478,7 @@ def run_ours(a):
     per = {}
     R = 4 * copies
     for k in kinds:
-        g = graph_of(lambda i, k=k: qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh), R, stream)
+        g = graph_of(lambda i, k=k: qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh, weights_const=True), R, stream)
         time_graph(g, 2, stream)
         ms = time_graph(g, max(5, 2000 // R), stream) / (R * max(5, 2000 // R))
         alg = wbytes[k] + 4 * K + 4 * M
@@ -502,7 +499,7 @@ def run_ours(a):
         for i in range(3):
             for k in kinds:
                 X[k].copy_(hx[k], non_blocking=True)
-                qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh)
+                qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh, weights_const=True)
                 hy[k].copy_(Y[k], non_blocking=True)
         torch.cuda.synchronize()
         e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -510,7 +507,7 @@ def run_ours(a):
         for i in range(n_e2e):
             for k in kinds:
                 X[k].copy_(hx[k], non_blocking=True)
-                qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh)
+                qmm.qgemv(k, W[k][i % copies], X[k], M, K, y=Y[k], stream=sh, weights_const=True)
                 hy[k].copy_(Y[k], non_blocking=True)
         e_e.record(stream)
         e_e.synchronize()
@@ -564,11 +561,10 @@ def run_case(a):
     from gemv_mul_mm_gb300 import qmm, synth
     what, _, arg = a.case.partition(":")
     if what == "gemv":
-        qmm.set_weight_prefetch(True)
         c = synth.DECODE
         W = torch.from_numpy(synth.workload_weights(c, arg)).cuda()
         x = torch.from_numpy(synth.workload_x(c, arg)).cuda()
-        fn = lambda: qmm.qgemv(arg, W, x, c["M"], c["K"])
+        fn = lambda: qmm.qgemv(arg, W, x, c["M"], c["K"], weights_const=True)
     elif what == "gemm":
         c = synth.KQUANT if arg in synth.KQUANT["kinds"] else synth.CODEBOOK
         W = torch.from_numpy(synth.workload_weights(c, arg)).cuda()

@@ -28,9 +28,8 @@ constexpr KindRow kKinds[QMM_NKINDS] = {
     {"IQ4_NL", 18, 32}, {"IQ4_XS", 136, 256}, {"MXFP4", 17, 32},
 };
 
-std::atomic<int> g_path{0};
-std::atomic<int> g_prefetch{0};
 std::atomic<uint64_t> g_launches{0};
+thread_local int t_path = 0;        // kernel-path override of the calling thread
 thread_local int t_last_path = 0;
 
 constexpr int kMaxDevices = 64;
@@ -81,8 +80,6 @@ int sm_count(int device) {
     }
     return g_sms[device];
 }
-
-bool weight_prefetch() { return g_prefetch.load(std::memory_order_relaxed) != 0; }
 
 bool encode_tiled_map(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
                       const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw,
@@ -162,16 +159,26 @@ const char* qmm_status_str(int status) {
 
 int qmm_set_path(int path) {
     if (path < 0 || path > 3) return -1;
-    return g_path.exchange(path);
+    const int prev = t_path;
+    t_path = path;
+    return prev;
 }
 
 int qmm_last_path(void) { return t_last_path; }
 
-int qmm_set_weight_prefetch(int on) { return g_prefetch.exchange(on ? 1 : 0); }
-
 uint64_t qmm_launch_count(void) { return g_launches.load(); }
 
-int qmm_shutdown(void) { return qmm::release_gemm_workspaces() ? QMM_OK : QMM_ERR_CUDA; }
+int qmm_shutdown(void) {
+    const bool ok = qmm::release_gemm_workspaces();
+    // device addresses of the library's __device__ arrays are looked up again
+    // on the next call (a new context may place them elsewhere)
+    qmm::forget_symbol_addresses();
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int d = 0; d < kMaxDevices; ++d) g_err_ptr[d] = nullptr;
+    }
+    return ok ? QMM_OK : QMM_ERR_CUDA;
+}
 
 int qdequant(int kind, const void* blocks, size_t blocks_bytes, int64_t rows, int64_t cols,
              float* out, size_t out_elems, void* stream) {
@@ -189,9 +196,10 @@ int qdequant(int kind, const void* blocks, size_t blocks_bytes, int64_t rows, in
                                  static_cast<cudaStream_t>(stream)), 4);
 }
 
-int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
-          float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream) {
+int qgemm_ex(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
+             float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, uint32_t flags, void* stream) {
     if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (flags & ~static_cast<uint32_t>(QMM_FLAG_WEIGHTS_CONST)) return QMM_ERR_BAD_ARGUMENT;
     if (M < 0 || K < 0 || N < 0) return QMM_ERR_BAD_ARGUMENT;
     if (M == 0 || K == 0 || N == 0) return QMM_ERR_EMPTY_SHAPE;
     if (!W || !X || !Y) return QMM_ERR_NULL_POINTER;
@@ -215,10 +223,11 @@ int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, s
     p.X = X;
     p.x_dtype = x_dtype;
     p.Y = Y;
+    p.flags = flags;
     p.err = err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    const int forced = g_path.load();
+    const int forced = t_path;
     if (forced == 1) return finish(launch_generic(p, s), 1);
     if (forced == 2) {
         if (!gemv_stream_ok(p)) return QMM_ERR_UNIMPLEMENTED;
@@ -233,9 +242,14 @@ int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, s
     return finish(launch_generic(p, s), 1);
 }
 
+int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
+          float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream) {
+    return qgemm_ex(kind, W, w_bytes, X, x_dtype, x_elems, Y, y_elems, M, K, N, 0u, stream);
+}
+
 int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_dtype, size_t x_elems,
           float* y, size_t y_elems, int64_t M, int64_t K, void* stream) {
-    return qgemm(kind, W, w_bytes, x, x_dtype, x_elems, y, y_elems, M, K, 1, stream);
+    return qgemm_ex(kind, W, w_bytes, x, x_dtype, x_elems, y, y_elems, M, K, 1, 0u, stream);
 }
 
 int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert_stride, int n_experts,
@@ -281,7 +295,7 @@ int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert_stride,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // every touched expert's rows stream once on the GEMV kernel; shapes it
     // does not take (unaligned rows, too many experts) run on the generic one
-    if (g_path.load() != 1 && gemv_stream_ok(p)) return finish(launch_gemv_stream(p, s), 5);
+    if (t_path != 1 && gemv_stream_ok(p)) return finish(launch_gemv_stream(p, s), 5);
     return finish(launch_generic(p, s), 1);
 }
 

@@ -43,6 +43,7 @@
 #include <mutex>
 
 #include "decode.cuh"
+#include "qmm.h"
 #include "qmm_internal.cuh"
 #include "sm100_async.cuh"
 #include "tc_fastdec.cuh"
@@ -918,9 +919,10 @@ bool release_workspaces() {
 
 template <int KIND>
 void ok_kind(const Problem& p, bool* out) {
+    // one CTA per tile puts the token tiles on grid.y (at most 65535 of them)
     *out = !p.x_row && p.x_dtype == 1 && p.K % KSUP == 0 && p.row_bytes % 16 == 0 &&
            reinterpret_cast<uintptr_t>(p.W) % 16 == 0 && reinterpret_cast<uintptr_t>(p.X) % 16 == 0 &&
-           p.M <= (int64_t(1) << 30) && p.N <= (int64_t(1) << 30) && p.K <= (int64_t(1) << 30);
+           p.M <= (int64_t(1) << 30) && (p.N + BN - 1) / BN <= 65535 && p.K <= (int64_t(1) << 30);
 }
 
 // QMM_TC_SPLIT: 0 = automatic, 1 = one tile per CTA always, 2 = shared
@@ -1042,7 +1044,8 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64] = {};
 
 // Device address of the scratch array on the current device, looked up once
-// per device (host code cannot use the array's name as a device address).
+// per device (host code cannot use the array's name as a device address) and
+// forgotten by qmm_shutdown.
 cudaError_t noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1072,19 +1075,19 @@ void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.X, K, N, static_cast<uint64_t>(K) * 2, KSUB, BN,
                   CU_TENSOR_MAP_SWIZZLE_128B)) {
-        *status = 10;  // QMM_ERR_CUDA
+        *status = QMM_ERR_CUDA;
         return;
     }
     tmB = tmX;
     if constexpr (MN::ON) {
         const size_t need = static_cast<size_t>(N) * nsup * MN::KMW * 2;
         if (need > kNoAllocScratchBytes) {
-            *status = 16;  // QMM_ERR_NOALLOC_LIMIT
+            *status = QMM_ERR_NOALLOC_LIMIT;
             return;
         }
         void* ws = nullptr;
         if (noalloc_scratch(&ws) != cudaSuccess) {
-            *status = 10;
+            *status = QMM_ERR_CUDA;
             return;
         }
         // k_xsums writes every entry of the region this call reads, so nothing
@@ -1098,13 +1101,13 @@ void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
         if (cudaGetLastError() != cudaSuccess ||
             !make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws, static_cast<uint64_t>(nsup) * MN::KMW, N,
                       static_cast<uint64_t>(nsup) * MN::KMW * 2, 16, BN, CU_TENSOR_MAP_SWIZZLE_32B)) {
-            *status = 10;
+            *status = QMM_ERR_CUDA;
             return;
         }
     }
     auto kern = k_gemm_tc<KIND>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) != cudaSuccess) {
-        *status = 10;
+        *status = QMM_ERR_CUDA;
         return;
     }
     TcArgs a;
@@ -1121,12 +1124,17 @@ void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
     const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);
     kern<<<grid, kThreads, L::BYTES, s>>>(tmW, tmX, tmB, a);
     count_launch(1);
-    if (cudaGetLastError() != cudaSuccess) *status = 10;
+    if (cudaGetLastError() != cudaSuccess) *status = QMM_ERR_CUDA;
 }
 
 }  // namespace
 
 bool release_gemm_workspaces() { return release_workspaces(); }
+
+void forget_symbol_addresses() {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    for (auto& p : g_noalloc_ptr) p = nullptr;
+}
 
 int launch_gemm_tc_noalloc(const Problem& p, cudaStream_t s) {
     int status = 0;

@@ -43,7 +43,8 @@
 //     packed subtract leaves q. Both multiply with packed fp32x2 FMAs; the fp32
 //     block scale multiplies the block's partial sum.
 //   * Programmatic dependent launch: the kernel lets the next one on the stream
-//     launch at once. When the caller declares the weights constant, each CTA
+//     launch at once. When the caller declares the weights constant
+//     (QMM_FLAG_WEIGHTS_CONST), each CTA
 //     of the next GEMV streams its first weight stages as soon as it is
 //     resident -- beside this kernel's CTAs when the stage ring fits two CTAs
 //     per SM, else as this kernel's CTAs retire -- while this one drains.
@@ -59,6 +60,7 @@
 #include <cuda_fp16.h>
 
 #include "decode.cuh"
+#include "qmm.h"
 #include "qmm_internal.cuh"
 #include "sm100_async.cuh"
 
@@ -993,7 +995,7 @@ cudaError_t launch_nc(const Problem& p, const Plan& pl, cudaStream_t s) {
     a.stride = pl.stride;
     a.upr = pl.upr;
     a.cpr = pl.cpr;
-    a.flags = (!p.x_row && weight_prefetch()) ? kFlagPrefetchW : 0;
+    a.flags = (!p.x_row && (p.flags & QMM_FLAG_WEIGHTS_CONST)) ? kFlagPrefetchW : 0;
     a.err = p.err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

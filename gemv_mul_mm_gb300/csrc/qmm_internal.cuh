@@ -20,9 +20,6 @@ enum : unsigned {
 // Number of streaming multiprocessors of `device` (cached).
 int sm_count(int device);
 
-// Whether callers declared their weights constant (qmm_set_weight_prefetch).
-bool weight_prefetch();
-
 // Records `n` kernel launches in the process-wide counter.
 void count_launch(int n);
 
@@ -48,6 +45,7 @@ struct Problem {
     size_t expert_stride = 0;
     int n_experts = 0;
     int64_t n_x_rows = 0;
+    unsigned flags = 0;      // QMM_FLAG_* of the call
     unsigned* err = nullptr; // device latch
 };
 
@@ -73,5 +71,7 @@ cudaError_t launch_gemm_tc(const Problem& p, cudaStream_t s);
 int launch_gemm_tc_noalloc(const Problem& p, cudaStream_t s);
 // Frees the GEMM's grown workspaces on every device; false if a free failed.
 bool release_gemm_workspaces();
+// Drops the cached device addresses of the library's __device__ arrays.
+void forget_symbol_addresses();
 
 }  // namespace qmm

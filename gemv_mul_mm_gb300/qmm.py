@@ -32,6 +32,7 @@ STATUS = {
 STATUS_ID = {v: k for k, v in STATUS.items()}
 
 PATH_AUTO, PATH_GENERIC, PATH_GEMV, PATH_TC, PATH_DEQUANT, PATH_GROUPED = 0, 1, 2, 3, 4, 5
+FLAG_WEIGHTS_CONST = 1
 
 
 class QmmError(RuntimeError):
@@ -61,13 +62,13 @@ def _lib():
         L.qdequant.argtypes = [_I, _P, _SZ, _I64, _I64, _P, _SZ, _P]
         L.qgemv.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _P]
         L.qgemm.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _I64, _P]
+        L.qgemm_ex.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _I64, ctypes.c_uint32, _P]
         L.qgemm_noalloc.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _I64, _P]
         L.qgemm_grouped.argtypes = [_I, _P, _SZ, _SZ, _I, _P, _I, _SZ, _I64, _P, _P, _I64,
                                     _P, _SZ, _I64, _I64, _P]
         L.qmm_check_device_error.argtypes = [_P]
         L.qmm_selftest_wait_timeout.argtypes = [_I64, _P]
         L.qmm_set_path.argtypes = [_I]
-        L.qmm_set_weight_prefetch.argtypes = [_I]
         L.qmm_launch_count.restype = ctypes.c_uint64
         L.qmm_shutdown.argtypes = []
         _LIB = L
@@ -118,12 +119,8 @@ def row_bytes(kind, K: int) -> int:
 
 
 def set_path(path: int) -> int:
+    """Kernel-path override of the calling thread (0 = automatic)."""
     return _lib().qmm_set_path(path)
-
-
-def set_weight_prefetch(on: bool) -> int:
-    """Declare weights constant while work is in flight (enables early weight streaming)."""
-    return _lib().qmm_set_weight_prefetch(1 if on else 0)
 
 
 def last_path() -> int:
@@ -152,13 +149,16 @@ def qdequant(kind, blocks, rows: int, cols: int, out=None, stream=None):
     return out
 
 
-def qgemm(kind, W, X, M: int, K: int, N: int, Y=None, stream=None):
-    """Y[n, m] = sum_k W[m, k] X[n, k]; returns Y as an (N, M) fp32 tensor."""
+def qgemm(kind, W, X, M: int, K: int, N: int, Y=None, stream=None, weights_const: bool = False):
+    """Y[n, m] = sum_k W[m, k] X[n, k]; returns Y as an (N, M) fp32 tensor.
+    weights_const: W is not written by work still in flight on the stream
+    (QMM_FLAG_WEIGHTS_CONST: the GEMV may start streaming it early)."""
     import torch
     if Y is None:
         Y = torch.empty((N, M), dtype=torch.float32, device=W.device)
-    _check(_lib().qgemm(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(X), _xdt(X),
-                        X.numel(), _ptr(Y), Y.numel(), M, K, N, _stream(stream)), "qgemm")
+    flags = FLAG_WEIGHTS_CONST if weights_const else 0
+    _check(_lib().qgemm_ex(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(X), _xdt(X),
+                           X.numel(), _ptr(Y), Y.numel(), M, K, N, flags, _stream(stream)), "qgemm")
     return Y
 
 
@@ -174,12 +174,18 @@ def qgemm_noalloc(kind, W, X, M: int, K: int, N: int, Y=None, stream=None):
     return Y
 
 
-def qgemv(kind, W, x, M: int, K: int, y=None, stream=None):
+def qgemv(kind, W, x, M: int, K: int, y=None, stream=None, weights_const: bool = False):
+    """y[m] = sum_k W[m, k] x[k] (qgemm with N = 1)."""
     import torch
     if y is None:
         y = torch.empty((M,), dtype=torch.float32, device=W.device)
-    _check(_lib().qgemv(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(x), _xdt(x),
-                        x.numel(), _ptr(y), y.numel(), M, K, _stream(stream)), "qgemv")
+    if weights_const:
+        _check(_lib().qgemm_ex(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(x), _xdt(x),
+                               x.numel(), _ptr(y), y.numel(), M, K, 1, FLAG_WEIGHTS_CONST,
+                               _stream(stream)), "qgemv")
+    else:
+        _check(_lib().qgemv(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(x), _xdt(x),
+                            x.numel(), _ptr(y), y.numel(), M, K, _stream(stream)), "qgemv")
     return y
 
 

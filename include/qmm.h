@@ -10,9 +10,12 @@
  *
  * Conventions shared by every entry point:
  *   - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA tensors)
- *     on the current CUDA device. The library never allocates on these paths and
- *     never takes ownership; the caller keeps every buffer alive until the work
- *     queued on `stream` has finished.
+ *     on the current CUDA device. The library never takes ownership; the caller
+ *     keeps every buffer alive until the work queued on `stream` has finished.
+ *     qdequant, qgemv, qgemm_grouped and qgemm_noalloc never allocate device
+ *     memory. qgemm (and qgemm_ex) with N > 8 on the tensor-core path may grow
+ *     a per-device workspace that the library owns (see qgemm); qmm_shutdown
+ *     frees it.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call
  *     is asynchronous with respect to the host: it validates, queues kernels on
  *     `stream` and returns.
@@ -167,30 +170,49 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
 QMM_API int qgemm(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
           float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, void* stream);
 
+/* Per-call flags of qgemm_ex. */
+enum {
+    /* W is not written by any work still in flight on `stream` (the normal
+     * case for model weights). The weight-streaming GEMV (N <= 8) may then
+     * start reading W while the preceding kernel on the stream is still
+     * running (programmatic dependent launch); activations are read, and
+     * outputs written, only after that kernel has completed, with or without
+     * the flag. Other paths ignore it. */
+    QMM_FLAG_WEIGHTS_CONST = 1
+};
+
+/*
+ * qgemm_ex -- qgemm with per-call flags (a bitwise OR of QMM_FLAG_* values;
+ * unknown bits are QMM_ERR_BAD_ARGUMENT). qgemm and qgemv are qgemm_ex with
+ * flags 0.
+ */
+QMM_API int qgemm_ex(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
+                     float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, uint32_t flags,
+                     void* stream);
+
 /*
  * qgemm_noalloc -- qgemm on the tensor-core path that never allocates device
- * memory. No passage of the pages has a counterpart: this entry point exists
- * for callers that cannot let a library call cudaMalloc -- code running while
- * its stream is being captured into a CUDA graph (an allocation there breaks
- * the capture), and runtimes that reserve all device memory up front and
- * hand out only their own pools.
+ * memory. The pages have no counterpart to it. It is for callers that cannot
+ * let a library call cudaMalloc: serving runtimes that reserve all of the
+ * GPU's memory at start-up and hand out only their own pools (a cudaMalloc
+ * from a library then fails or steals from the pool), and callers on a hot
+ * path where an allocation's implicit device synchronisation is not allowed.
  *
  * It computes what qgemm computes, with the same arguments, layouts and
  * accuracy (one CTA per output tile, never shared K ranges, so the rounding
  * of the sums can differ from qgemm's), but only on the tensor-core path:
- * f16 activations, K a
- * multiple of 256, 16-byte aligned W and X, rows a multiple of 16 bytes
- * (QMM_ERR_UNIMPLEMENTED otherwise). The per-group activation sums that
- * Q4_K, Q5_K and Q2_K need go to a fixed 4 MiB device array compiled into the
- * library (held on every GPU that loads it, until the process exits) instead
- * of a grown workspace; a problem whose sums need more,
- * N * (K / 256) * 32 bytes for Q4_K / Q5_K or N * (K / 256) * 64 bytes for
- * Q2_K above 4 MiB, returns QMM_ERR_NOALLOC_LIMIT before anything is launched.
- * Each call rewrites all the scratch it reads. The array is shared by every
- * call: calls that can overlap on the GPU (different streams, same device)
- * race on it and must be ordered by the caller. The first call on a device
- * looks the array's address up (cudaGetSymbolAddress, no allocation); make
- * that first call before any stream capture.
+ * f16 activations, K a multiple of 256, 16-byte aligned W and X, rows a
+ * multiple of 16 bytes (QMM_ERR_UNIMPLEMENTED otherwise). The per-group
+ * activation sums that Q4_K, Q5_K and Q2_K need go to a fixed 4 MiB device
+ * array compiled into the library (held on every GPU that loads it, until
+ * the process exits) instead of a grown workspace; a problem whose sums need
+ * more, N * (K / 256) * 32 bytes for Q4_K / Q5_K or N * (K / 256) * 64 bytes
+ * for Q2_K above 4 MiB, returns QMM_ERR_NOALLOC_LIMIT before anything is
+ * launched. Each call rewrites all the scratch it reads, so nothing is left
+ * to clear between calls. The array is shared by every call: calls that can
+ * overlap on the GPU (different streams, same device) race on it and must
+ * be ordered by the caller. The first call on a device looks the array's
+ * address up with cudaGetSymbolAddress (no allocation), once per device.
  */
 QMM_API int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype,
                           size_t x_elems, float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N,
@@ -248,17 +270,10 @@ QMM_API int qmm_selftest_wait_timeout(int64_t cycles, void* stream);
 
 /* Kernel-path override, for tests and experiments: 0 = automatic (default),
  * 1 = force the generic CUDA-core kernels, 2 = force the streaming GEMV for
- * qgemm (N <= 8), 3 = force the tensor-core GEMM for qgemm. Returns the
- * previous value, or -1 for an unknown value (setting unchanged). Process-wide. */
+ * qgemm (N <= 8), 3 = force the tensor-core GEMM for qgemm. Applies to the
+ * later calls of the calling host thread only (thread-local). Returns that
+ * thread's previous value, or -1 for an unknown value (setting unchanged). */
 QMM_API int qmm_set_path(int path);
-
-/* Declares that weight buffers passed to later calls are not written by work
- * still in flight on the same stream (the normal case for model weights).
- * The streaming GEMV then starts reading W while the preceding kernel on the
- * stream is still running (programmatic dependent launch); activations are
- * read, and outputs written, only after that kernel has completed in either
- * mode. Process-wide; default 0. Returns the previous value. */
-QMM_API int qmm_set_weight_prefetch(int on);
 
 /* Which kernel family the most recent successful call on this host thread
  * launched: 1 generic, 2 streaming GEMV, 3 tensor-core GEMM, 4 dequant,
@@ -270,11 +285,15 @@ QMM_API uint64_t qmm_launch_count(void);
 
 /*
  * qmm_shutdown -- frees the per-device workspaces qgemm grows (activation
- * sums, partial tiles; see qgemm) on every device that has one. cudaFree
- * waits for the work in flight on that device first. Later calls grow them
- * again as needed. Not to be called while another thread is inside the
- * library. Returns QMM_OK, or QMM_ERR_CUDA if a free failed (the remaining
- * ones are still attempted). The current device is left as it was.
+ * sums, partial tiles; see qgemm) on every device that has one, and forgets
+ * the device addresses of the library's own device arrays (its error latch
+ * and qgemm_noalloc's scratch), which the next call looks up again. cudaFree
+ * waits for the work in flight on that device first. Later calls grow the
+ * workspaces again as needed. Call it before anything that tears down a
+ * device's context (cudaDeviceReset): addresses cached across that would be
+ * stale. Not to be called while another thread is inside the library.
+ * Returns QMM_OK, or QMM_ERR_CUDA if a free failed (the remaining ones are
+ * still attempted). The current device is left as it was.
  */
 QMM_API int qmm_shutdown(void);
 

@@ -107,11 +107,28 @@ def test_grouped_refusals(L):
     assert g(ye=3 * 64 - 1) == S["QMM_ERR_OUTPUT_TOO_SMALL"]
 
 
-def test_path_override(L):
+def test_path_override_is_per_thread(L):
+    import threading
     assert qmm.set_path(1) == 0
-    assert qmm.set_path(0) == 1
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(qmm.set_path(2)))
+    t.start()
+    t.join()
+    assert seen == [0]                 # another thread starts from the default
+    assert qmm.set_path(0) == 1        # and did not change this thread's setting
     assert qmm.set_path(9) == -1
     assert qmm.set_path(0) == 0
+
+
+def test_qgemm_ex_flags(L):
+    S = qmm.STATUS_ID
+    args = (1, FAKE, 1 << 30, FAKE, 0, 1 << 30, FAKE, 1 << 30, 64, 256)
+    # unknown flag bits are refused before anything else is looked at
+    assert L.qgemm_ex(*args, 1, 2, None) == S["QMM_ERR_BAD_ARGUMENT"]
+    assert L.qgemm_ex(*args, 1, 0x80000000, None) == S["QMM_ERR_BAD_ARGUMENT"]
+    # the known flag passes validation like qgemm (refused later for the shape)
+    assert L.qgemm_ex(1, FAKE, 1 << 30, FAKE, 0, 1 << 30, FAKE, 1 << 30, 64, 48, 1,
+                      qmm.FLAG_WEIGHTS_CONST, None) == S["QMM_ERR_COLS_NOT_BLOCK_ALIGNED"]
 
 
 def test_selftest_refuses_bad_cycle_counts(L):

@@ -35,10 +35,17 @@ def test_comment_edit_keeps_hash_code_edit_changes_it():
     assert s(base) != s(changed)
 
 
-def test_committed_traffic_matches_current_gemv_sources():
-    # the committed DRAM counters were taken on the kernel as it is now
-    assert bench.traffic_for("k_gemv<Q8_0>", ["k_gemv.cu", "decode.cuh", "sm100_async.cuh"]) == 62510336
-    assert bench.traffic_for("k_gemv<Q4_0>", ["k_gemv.cu", "decode.cuh", "sm100_async.cuh"]) == 33130240
+def test_traffic_counters_only_for_the_kernel_they_were_taken_on(tmp_path):
+    # counters recorded under the current sources' hash are returned; under
+    # any other hash (the kernel changed since) the figure is None
+    import json
+    srcs = ["k_gemv.cu", "decode.cuh", "sm100_async.cuh"]
+    p = tmp_path / "traffic.json"
+    p.write_text(json.dumps({"k_gemv<Q8_0>": {"dram_bytes_per_launch": 123, "src_sha": bench.src_hash(*srcs)},
+                             "k_gemv<Q4_0>": {"dram_bytes_per_launch": 456, "src_sha": "0" * 16}}))
+    assert bench.traffic_for("k_gemv<Q8_0>", srcs, str(p)) == 123
+    assert bench.traffic_for("k_gemv<Q4_0>", srcs, str(p)) is None
+    assert bench.traffic_for("k_gemv<Q5_0>", srcs, str(p)) is None
 
 
 def test_reference_arm_json_line_keeps_the_contract():

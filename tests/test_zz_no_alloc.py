@@ -1,11 +1,14 @@
-"""qgemm_noalloc against qgemm, called through the C ABI.
+"""qgemm_noalloc, called through the C ABI, against the oracle and against qgemm.
 
-qgemm_noalloc is the entry point for callers that must not let the library
-allocate device memory -- code whose stream is being captured into a CUDA
-graph, or a runtime that reserves all device memory up front. It keeps its
-scratch in a fixed device array instead of a grown workspace. It must give the
-same answer as qgemm within the suite's tolerance, also on a second call right
-after a first one (the array still holds the first call's contents).
+qgemm_noalloc is the entry point for callers that cannot let the library
+allocate device memory: serving runtimes that reserve all of the GPU's memory
+at start-up and hand out only their own pools, and hot paths where an
+allocation's implicit device synchronisation is not allowed. It keeps its
+scratch in a fixed device array instead of a grown workspace. Every output
+must match the oracle within the suite's tolerance, and the existing entry
+point (qgemm) within the same tolerance, also on the second of two calls in a
+row (the array still holds the first call's contents). This file is collected
+last, so a run that stops at the first failure has run every other test.
 """
 import ctypes
 
@@ -37,7 +40,7 @@ def _noalloc(Q, kind, W, X, Y, M, K, N):
 
 
 @pytest.mark.parametrize("kind", ["Q4_K", "Q2_K", "Q5_K", "IQ4_NL"])
-def test_noalloc_matches_qgemm_on_two_calls_in_a_row(Q, orc, kind):
+def test_noalloc_matches_oracle_and_qgemm_on_two_calls_in_a_row(Q, orc, kind):
     import torch
     problems = [(384, 2048, 160, 11), (256, 4096, 96, 12)]   # (M, K, N, seed)
     outs = []
@@ -52,13 +55,13 @@ def test_noalloc_matches_qgemm_on_two_calls_in_a_row(Q, orc, kind):
     assert Q.check_device_error() == 0
     for w, x, Wd, Xd, Yn, M, K, N in outs:
         Yq = Q.qgemm(kind, Wd, Xd, M, K, N)
-        got, want = Yn.cpu().numpy(), Yq.cpu().numpy()
+        got, other = Yn.cpu().numpy().astype(np.float64), Yq.cpu().numpy().astype(np.float64)
         assert not np.any(got == -1e30), "output not fully written"
-        n_idx = np.arange(N).repeat(4)[:400] % N
-        m_idx = (np.arange(n_idx.size) * 37) % M
-        _, tol = orc.gemm_at(kind, w, M, K, x, n_idx, m_idx)
-        assert np.all(np.abs(got[n_idx, m_idx] - want[n_idx, m_idx]) <= tol)
-        assert np.allclose(got, want, rtol=1e-3, atol=1e-3)
+        y, tol = orc.gemm(kind, w, M, K, x, N)
+        bad = ~(np.abs(got - y) <= tol)
+        assert not bad.any(), f"{int(bad.sum())} outputs outside the oracle's tolerance"
+        bad = ~(np.abs(got - other) <= tol)
+        assert not bad.any(), f"{int(bad.sum())} outputs differ from qgemm's by more than the tolerance"
 
 
 def test_noalloc_refuses_oversize_and_unsupported(Q):
