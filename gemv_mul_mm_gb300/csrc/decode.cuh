@@ -146,6 +146,113 @@ __device__ __forceinline__ float elem(const uint8_t* b, int e) {
     return elem32<KIND>(b, e >> 5, e & 31);
 }
 
+// Elements e .. e + 3 (e a multiple of 4) of the block at b, the same values
+// as elem() bit for bit: the four share one scale group (every format's
+// groups are 16 or 32 elements), so the scale factors are derived once. The
+// codebook formats read their table from `tbl` (16 floats: the IQ4_NL values,
+// or E2M1 for MXFP4), a copy the caller keeps in shared memory -- one entry
+// per bank, so lanes with different codes never serialize, as they do on a
+// per-lane-indexed __constant__ array. Byte loads only (any alignment).
+template <int KIND>
+__device__ __forceinline__ float4 elem4(const uint8_t* b, int e, const float* tbl) {
+    float v[4];
+    const int j = e >> 5, i0 = e & 31;
+    if constexpr (KIND == Q8_0) {
+        const float d = h2f(ld16(b, 0));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = d * static_cast<float>(static_cast<int8_t>(b[2 + i0 + t]));
+    } else if constexpr (KIND == Q4_0 || KIND == IQ4_NL) {
+        const float d = h2f(ld16(b, 0));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const uint32_t byte = b[2 + (i & 15)];
+            const int c = (i < 16) ? (byte & 15) : (byte >> 4);
+            v[t] = (KIND == Q4_0) ? d * static_cast<float>(c - 8) : d * tbl[c];
+        }
+    } else if constexpr (KIND == Q5_0) {
+        const float d = h2f(ld16(b, 0));
+        const uint32_t qh = ld8(b, 2) | (ld8(b, 3) << 8) | (ld8(b, 4) << 16) | (ld8(b, 5) << 24);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const uint32_t byte = b[6 + (i & 15)];
+            const int lo = static_cast<int>((i < 16) ? (byte & 15) : (byte >> 4));
+            const int q = lo | static_cast<int>(((qh >> i) & 1u) << 4);   // signed: q - 16 may be negative
+            v[t] = d * static_cast<float>(q - 16);
+        }
+    } else if constexpr (KIND == Q4_K || KIND == Q5_K) {
+        int sc, mn;
+        k4_sm(b + 4, j, sc, mn);
+        const float ds = h2f(ld16(b, 0)) * static_cast<float>(sc);
+        const float dm = h2f(ld16(b, 2)) * static_cast<float>(mn);
+        const int qs = (KIND == Q4_K) ? 16 : 48;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const uint32_t byte = b[qs + (j >> 1) * 32 + i];
+            int q = (j & 1) ? (byte >> 4) : (byte & 15);
+            if constexpr (KIND == Q5_K) q += ((b[16 + i] >> j) & 1) << 4;
+            v[t] = __fsub_rn(__fmul_rn(ds, static_cast<float>(q)), dm);
+        }
+    } else if constexpr (KIND == Q6_K) {
+        const int h = j >> 2, g = j & 3;
+        const float ds = h2f(ld16(b, 208)) * static_cast<float>(static_cast<int8_t>(b[192 + 2 * j + (i0 >> 4)]));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const uint32_t lob = b[h * 64 + i + (g & 1) * 32];
+            const int lo = (g >= 2) ? (lob >> 4) : (lob & 15);
+            const int hi = (b[128 + h * 32 + i] >> (2 * g)) & 3;
+            v[t] = ds * static_cast<float>((lo | (hi << 4)) - 32);
+        }
+    } else if constexpr (KIND == Q2_K) {
+        const int h = j >> 2, g = j & 3;
+        const int s = b[2 * j + (i0 >> 4)];
+        const float dl = h2f(ld16(b, 80)) * static_cast<float>(s & 15);
+        const float ml = h2f(ld16(b, 82)) * static_cast<float>(s >> 4);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int q = (b[16 + h * 32 + i0 + t] >> (2 * g)) & 3;
+            v[t] = __fsub_rn(__fmul_rn(dl, static_cast<float>(q)), ml);
+        }
+    } else if constexpr (KIND == Q3_K) {
+        const int h = j >> 2, g = j & 3;
+        const float ds = h2f(ld16(b, 108)) * static_cast<float>(q3_scale(b + 96, 2 * j + (i0 >> 4)) - 32);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const int q2 = (b[32 + h * 32 + i] >> (2 * g)) & 3;
+            v[t] = ds * static_cast<float>(q2 - (((b[i] >> j) & 1) ? 0 : 4));
+        }
+    } else if constexpr (KIND == IQ4_XS) {
+        const uint32_t sh = ld16(b, 2);
+        const int ls = ((b[4 + (j >> 1)] >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4);
+        const float ds = h2f(ld16(b, 0)) * static_cast<float>(ls - 32);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const uint32_t byte = b[8 + 16 * j + (i & 15)];
+            v[t] = ds * tbl[(i < 16) ? (byte & 15) : (byte >> 4)];
+        }
+    } else {  // MXFP4
+        const float s = e8m0f(b[0]);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const uint32_t byte = b[1 + (i & 15)];
+            v[t] = s * tbl[(i < 16) ? (byte & 15) : (byte >> 4)];
+        }
+    }
+    return make_float4(v[0], v[1], v[2], v[3]);
+}
+
+// The 16-entry table elem4 reads for a format (nullptr-safe for the others).
+template <int KIND>
+__device__ __forceinline__ float codebook_entry(int c) {
+    return KIND == MXFP4 ? c_kv_e2m1[c] : c_kv_iq4nl[c];
+}
+
 
 // ---------------------------------------------------------------------------
 // Tensor-core operand decoding: integer codes (times integer sub-scales) and

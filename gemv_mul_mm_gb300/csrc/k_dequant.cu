@@ -5,8 +5,10 @@
 // bytes (a multiple of 16 for every format) are staged into shared memory with
 // coalesced 16-byte loads, then each thread decodes two float4 of output and
 // writes them with coalesced 16-byte stores (256 threads x 16 B = 4 KB per
-// store wave). The write of 4 bytes per element dominates the traffic, so the
-// roofline is HBM: bytes = blocks + 4 * elements.
+// store wave). Each float4 is one call of elem4, which derives the group's
+// scale factors once for its four elements; codebooks are read from a copy in
+// shared memory. The write of 4 bytes per element dominates the traffic, so
+// the roofline is HBM: bytes = blocks + 4 * elements.
 //
 // Element values: Vulkore examples/llm/quant_test.cpp (the `ref::` CPU
 // references, element-indexed) and ferrox-cuda 0.20.0 codebook.rs.
@@ -27,6 +29,8 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict_
     constexpr int TBYTES = TB * BB;            // multiple of 16 for every format
     static_assert(TBYTES % 16 == 0, "tile bytes must be whole 16-byte vectors");
     __shared__ __align__(16) uint8_t sbuf[TBYTES];
+    __shared__ float tbl[16];   // codebook (IQ4_NL / IQ4_XS / MXFP4), one entry per bank
+    if (threadIdx.x < 16) tbl[threadIdx.x] = codebook_entry<KIND>(threadIdx.x);
 
     const int64_t ntiles = (nblocks + TB - 1) / TB;
     const int64_t total_elems = nblocks * BE;
@@ -48,12 +52,7 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict_
             const int e = 4 * threadIdx.x + half * (kTileElems / 2);
             const int blk = e / BE, eb = e % BE;
             if (blk < nb) {
-                const uint8_t* b = sbuf + blk * BB;
-                float4 v;
-                v.x = elem<KIND>(b, eb + 0);
-                v.y = elem<KIND>(b, eb + 1);
-                v.z = elem<KIND>(b, eb + 2);
-                v.w = elem<KIND>(b, eb + 3);
+                const float4 v = elem4<KIND>(sbuf + blk * BB, eb, tbl);
                 float* dst = out + e_base + e;
                 if (vec_out) {
                     __stcs(reinterpret_cast<float4*>(dst), v);

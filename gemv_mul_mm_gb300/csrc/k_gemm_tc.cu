@@ -52,6 +52,7 @@ namespace qmm {
 namespace {
 
 constexpr int BM = 128, BN = 128, KSUP = 256, KSUB = 64;
+static_assert(KSUB == 64, "a sub-step is four K = 16 MMAs: two 32-element blocks");
 constexpr int kProdWarp = 0, kMmaWarp = 1, kNumDec = 4, kEpi0 = 6, kNumEpi = 8;   // decoders: warps 2-5
 constexpr int kXWarp = kEpi0 + kNumEpi;           // activation-tile producer
 constexpr int kWaitWarp = kXWarp + 1;             // waits on behalf of the MMA issuer
@@ -512,7 +513,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // waiter warp, which hands each ready sub-step over through a named
         // barrier (bar.red also carries whether to go on).
         const int nloc = cta_span(a).n;
+        // Shared-memory descriptors are built once: the activation stages are
+        // 1024-byte aligned and end below 2^18, so the descriptor of base + o
+        // is the base's plus o / 16 in its address field (no carry). Building
+        // one in front of every MMA measured 94-118 cycles per MMA against
+        // the 64 of one issued back to back.
+        const uint64_t xdesc0 = desc_sw128(smem_u32(x_tiles));
         int sub = 0;
+        int ub = 0;   // per-32 formats: accumulator of the sub-step's first 32-element block
         for (int s = 0; s < nloc; ++s) {
             for (int q = 0; q < KSUP / KSUB; ++q, ++sub) {
                 const bool go = bar_red_and(kBarHand + (sub & 1), 64, true);
@@ -520,18 +528,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const int as = sub % AS, xs = (sub >> 1) % XS;
                     const uint32_t a_tm = tmem + as * kACols;
-                    const uint32_t xbase = smem_u32(x_tiles + xs * X_TILE + (sub & 1) * X_SUB);
+                    const uint64_t xd = xdesc0 + static_cast<uint32_t>((xs * X_TILE + (sub & 1) * X_SUB) >> 4);
+                    if constexpr (PER32) {
+                        const int b1 = (ub + 1 == ND) ? 0 : ub + 1;
+                        const uint32_t d0 = tmem + kDCol0 + ub * BN, d1 = tmem + kDCol0 + b1 * BN;
+                        tc_mma_ts(d0, a_tm, xd, kIdesc, 0u);
+                        tc_mma_ts(d0, a_tm + 8, xd + 2, kIdesc, 1u);
+                        tc_commit(&d_full[ub]);
+                        tc_mma_ts(d1, a_tm + 16, xd + 4, kIdesc, 0u);
+                        tc_mma_ts(d1, a_tm + 24, xd + 6, kIdesc, 1u);
+                        tc_commit(&d_full[b1]);
+                    } else {
+                        const uint32_t d = tmem + kDCol0 + (s & 1) * BN;
 #pragma unroll
-                    for (int kk = 0; kk < KSUB / 16; ++kk) {
-                        if constexpr (PER32) {
-                            const int b = (8 * s + 2 * q + (kk >> 1)) % ND;
-                            tc_mma_ts(tmem + kDCol0 + b * BN, a_tm + 8 * kk, desc_sw128(xbase + 32 * kk), kIdesc,
-                                      kk & 1);
-                            if (kk & 1) tc_commit(&d_full[b]);
-                        } else {
-                            tc_mma_ts(tmem + kDCol0 + (s & 1) * BN, a_tm + 8 * kk, desc_sw128(xbase + 32 * kk),
-                                      kIdesc, (q | kk) != 0);
-                        }
+                        for (int kk = 0; kk < KSUB / 16; ++kk)
+                            tc_mma_ts(d, a_tm + 8 * kk, xd + 2 * kk, kIdesc, (q | kk) != 0);
                     }
                     tc_commit(&a_empty[as]);
                     if (sub & 1) tc_commit(&x_empty[xs]);
@@ -551,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                if constexpr (PER32) ub = (ub + 2) % ND;
                 __syncwarp();
             }
         }
@@ -784,6 +796,374 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// The formats with one fp32 scale per 256-element super-block (Q4_K, Q5_K,
+// Q6_K, Q2_K, Q3_K, IQ4_XS) run a leaner pipeline, k_gemm_sb. Its unit is a
+// half-step: two sub-steps (K = 128, eight MMAs). Each half-step's MMAs end
+// with ONE tcgen05.commit on the stage's `done` barrier, which releases at
+// once everything the half-step read -- its A stage in tensor memory, its
+// activation stage (and, on the second half of a super-step, the min-term
+// tiles) -- and, on the second half, tells the epilogue that the super-step's
+// accumulators are complete. Measured on a lone issuing thread, every commit
+// costs the tensor pipe about 80 cycles (a group of four N = 128 MMAs takes
+// 256); the per-sub-step kernel above commits seven to nine times per
+// super-step, this one twice.
+//
+// Tensor memory (512 columns):
+//   formats with mins: A stages [0, 128) (two of 64 columns), D1 double
+//                      buffered at 128 and 256, the min term D2 at 384;
+//   the others:        A stages [0, 256) (four), D1 at 256 and 384.
+// A waiter on a barrier never falls two phases behind: the decoders and the
+// activation producer refill a stage only after its previous use completed;
+// the epilogue reads super-step s before the waiter lets the second half of
+// super-step s + 1 issue (that half waits for the epilogue's d_empty of s).
+// ---------------------------------------------------------------------------
+constexpr int kHalfSubs = 2;                   // sub-steps per half-step
+constexpr int kACols2 = kHalfSubs * kACols;    // 64 TMEM columns per A stage
+constexpr int X_HALF = kHalfSubs * X_SUB;      // 32 KB activation stage
+
+template <int KIND> struct PipeSB {
+    static constexpr bool MINS = Mins<KIND>::ON;
+    static constexpr int NS = MINS ? 2 : 4;                   // stages (A in TMEM, X in SMEM)
+    static constexpr int D1COL = NS * kACols2;                // 128 or 256
+    static constexpr int D2COL = D1COL + 2 * BN;              // 384 (formats with mins)
+    static constexpr int MINB = Mins<KIND>::TILES * MIN_TILE;
+    static constexpr int RAWB = BM * Raw<KIND>::BOXB;
+    static constexpr int FIXED = NS * X_HALF + 2 * MINB + 2 * BM * 8 * 4 + 2048;
+    static constexpr int FREE = 226 * 1024 - FIXED;
+    static constexpr int RS = FREE >= 4 * RAWB ? 4 : FREE >= 3 * RAWB ? 3 : 2;
+    static_assert(FIXED + RS * RAWB <= 226 * 1024, "shared memory");
+    static_assert(D1COL + 2 * BN <= kTmemCols && (!MINS || D2COL + BN <= kTmemCols), "tensor memory");
+};
+
+template <int KIND>
+struct LayoutSB {
+    using P = PipeSB<KIND>;
+    static constexpr int OFF_X = 0;                                      // 1024-aligned stages
+    static constexpr int OFF_RAW = OFF_X + P::NS * X_HALF;
+    static constexpr int OFF_AMIN = (OFF_RAW + P::RS * P::RAWB + 1023) & ~1023;
+    static constexpr int OFF_BMIN = OFF_AMIN + P::MINB;
+    static constexpr int OFF_SC = OFF_BMIN + P::MINB;                    // [2][128][8] floats
+    static constexpr int OFF_BAR = OFF_SC + 2 * BM * 8 * 4;
+    // raw_full/empty[RS], a_full[NS], x_full[NS], done[NS], d_empty, sc_full/empty[2], fin
+    static constexpr int NBAR = 2 * P::RS + 3 * P::NS + 1 + 4 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16 + 1024;                   // + alignment slack
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_sb(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const __grid_constant__ CUtensorMap tmB, TcArgs a) {
+    using R = Raw<KIND>;
+    using MN = Mins<KIND>;
+    using P = PipeSB<KIND>;
+    using L = LayoutSB<KIND>;
+    static_assert(!TcGeo<KIND>::PER32, "super-block formats only");
+    constexpr int NS = P::NS, RS = P::RS;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* x_tiles = smem + L::OFF_X;
+    uint8_t* raw = smem + L::OFF_RAW;
+    uint8_t* amin = smem + L::OFF_AMIN;
+    uint8_t* bmin = smem + L::OFF_BMIN;
+    float* sbuf = reinterpret_cast<float*>(smem + L::OFF_SC);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+    uint64_t* raw_full = bars;
+    uint64_t* raw_empty = raw_full + RS;
+    uint64_t* a_full = raw_empty + RS;
+    uint64_t* x_full = a_full + NS;
+    uint64_t* done = x_full + NS;
+    uint64_t* d_empty = done + NS;
+    uint64_t* sc_full = d_empty + 1;
+    uint64_t* sc_empty = sc_full + 2;
+    uint64_t* fin = sc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RS; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], kNumDec);
+        }
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&a_full[i], kNumDec);
+            mbar_init(&x_full[i], 1);
+            mbar_init(&done[i], 1);
+        }
+        mbar_init(d_empty, kNumEpi);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sc_full[i], kNumDec);
+            mbar_init(&sc_empty[i], kNumEpi);
+        }
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProdWarp) {
+        // ------------------------------------------------ TMA producer: raw weights
+        if (lane == 0) {
+            const Span span = cta_span(a);
+            const int nloc = span.n;
+            int s_issued = 0;
+            Step st(a, span);
+            for (int s = 0; s < nloc; ++s, st.next(a)) {
+                const int rs = s % RS;
+                if (s >= RS && !wait_bar(&raw_empty[rs], ((s / RS) - 1) & 1, abort_flag, a.err)) break;
+                mbar_arrive_expect_tx(&raw_full[rs], R::STAGE);
+                tma2d(raw + rs * R::STAGE, &tmW, ((st.s * R::SBB) & ~15) / 2, st.m0, &raw_full[rs]);
+                s_issued = s + 1;
+            }
+            for (int s = (s_issued > RS ? s_issued - RS : 0); s < s_issued; ++s)
+                drain_bar(&raw_full[s % RS], (s / RS) & 1, a.err);
+        }
+    } else if (warp == kXWarp) {
+        // ------------------------------------------------ TMA producer: activations (+ their group sums)
+        if (lane == 0) {
+            const Span span = cta_span(a);
+            const int nh = 2 * span.n;
+            int h = 0;
+            Step st(a, span);
+            for (; h < nh; ++h) {
+                const int half = h & 1, i = h % NS;
+                if (h > 0 && half == 0) st.next(a);
+                if (h >= NS && !wait_bar(&done[i], ((h / NS) - 1) & 1, abort_flag, a.err)) break;
+                const int k0 = st.s * KSUP + half * kHalfSubs * KSUB;
+                mbar_arrive_expect_tx(&x_full[i], X_HALF + ((MN::ON && half) ? P::MINB : 0));
+                tma2d(x_tiles + i * X_HALF, &tmX, k0, st.n0, &x_full[i]);
+                tma2d(x_tiles + i * X_HALF + X_SUB, &tmX, k0 + KSUB, st.n0, &x_full[i]);
+                if constexpr (MN::ON) {
+                    // the min term's activation sums ride with the super-step's
+                    // second half (single buffer: the previous super-step's min
+                    // MMA completed with the stage's previous use)
+                    if (half) {
+#pragma unroll
+                        for (int t = 0; t < MN::TILES; ++t)
+                            tma2d(bmin + t * MIN_TILE, &tmB, st.s * MN::KMW + 16 * t, st.n0, &x_full[i]);
+                    }
+                }
+            }
+            for (int j = (h > NS ? h - NS : 0); j < h; ++j) drain_bar(&x_full[j % NS], (j / NS) & 1, a.err);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        // Never touches shared memory between MMAs: the waiter warp hands each
+        // ready half-step over through a named barrier.
+        const int nh = 2 * cta_span(a).n;
+        const uint64_t xdesc0 = desc_sw128(smem_u32(x_tiles));
+        uint64_t adesc[MN::TILES > 0 ? MN::TILES : 1], bdesc[MN::TILES > 0 ? MN::TILES : 1];
+#pragma unroll
+        for (int t = 0; t < MN::TILES; ++t) {
+            adesc[t] = desc_sw32(smem_u32(amin + t * MIN_TILE));
+            bdesc[t] = desc_sw32(smem_u32(bmin + t * MIN_TILE));
+        }
+        for (int h = 0; h < nh; ++h) {
+            const bool go = bar_red_and(kBarHand + (h & 1), 64, true);
+            if (go && lane == 0) {
+                tc_fence_after();
+                const int i = h % NS, half = h & 1;
+                const uint32_t a_tm = tmem + i * kACols2;
+                const uint64_t xd = xdesc0 + static_cast<uint32_t>((i * X_HALF) >> 4);
+                const uint32_t d = tmem + P::D1COL + ((h >> 1) & 1) * BN;
+#pragma unroll
+                for (int sub = 0; sub < kHalfSubs; ++sub)
+#pragma unroll
+                    for (int kk = 0; kk < KSUB / 16; ++kk)
+                        tc_mma_ts(d, a_tm + sub * kACols + 8 * kk, xd + sub * (X_SUB >> 4) + 2 * kk, kIdesc,
+                                  (half | sub | kk) != 0);
+                if constexpr (MN::ON) {
+                    if (half) {
+#pragma unroll
+                        for (int t = 0; t < MN::TILES; ++t) tc_mma(tmem + P::D2COL, adesc[t], bdesc[t], kIdesc, t);
+                    }
+                }
+                tc_commit(&done[i]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            tc_commit(fin);
+            drain_bar(fin, 0, a.err);
+        }
+        __syncwarp();
+    } else if (warp == kWaitWarp) {
+        // ------------------------------------------------------------ MMA waiter
+        const int nh = 2 * cta_span(a).n;
+        bool ok = true;
+        for (int h = 0; h < nh; ++h) {
+            if (lane == 0 && ok) {
+                const int i = h % NS, u = h / NS, s = h >> 1;
+                ok = spin_bar(&a_full[i], u & 1, abort_flag, a.err);
+                if (ok) ok = spin_bar(&x_full[i], u & 1, abort_flag, a.err);
+                // the second half of super-step s rewrites the min term and
+                // completes D1[s & 1]: the epilogue must be done with s - 1
+                if (ok && (h & 1) && s >= 1) ok = spin_bar(d_empty, (s - 1) & 1, abort_flag, a.err);
+            }
+            bar_red_and(kBarHand + (h & 1), 64, lane != 0 || ok);
+        }
+    } else if (warp < kEpi0) {
+        // ------------------------------------------------------------ decoders
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const Span span = cta_span(a);
+        const int nloc = span.n;
+        int ks = span.s0;
+        for (int s = 0; s < nloc; ++s, ks = (ks + 1 == a.nsup) ? 0 : ks + 1) {
+            const int rs = s % RS;
+            bool ok = warp_wait_bar(&raw_full[rs], (s / RS) & 1, abort_flag, a.err);
+            const uint8_t* row = raw + rs * R::STAGE + r * R::BOXB + ((ks * R::SBB) & 15);
+            if (ok && s >= 2) ok = warp_wait_bar(&sc_empty[s & 1], ((s >> 1) - 1) & 1, abort_flag, a.err);
+            if (ok) {
+                const float2 dd = scale256<KIND>(row);
+                float* sc = sbuf + ((s & 1) * BM + r) * 8;
+                sc[0] = dd.x;
+                sc[1] = dd.y;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sc_full[s & 1]);
+            uint32_t scw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            if (ok) FastDec<KIND>::pre(row, scw);
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                const int h = 2 * s + half, i = h % NS;
+                uint32_t o[kHalfSubs][32];
+                if (ok) {
+                    FastDec<KIND>::sub_pre(row, 2 * half, o[0], scw);
+                    FastDec<KIND>::sub_pre(row, 2 * half + 1, o[1], scw);
+                }
+                // decode first, then wait for the stage, so the decode stays off
+                // the stage's round trip (ok is warp-uniform: tcgen05.st is
+                // warp-collective)
+                if (ok && h >= NS) ok = warp_wait_bar<true>(&done[i], ((h / NS) - 1) & 1, abort_flag, a.err);
+                if constexpr (MN::ON) {
+                    if (half && ok) {
+                        // A_min tile(s) of super-step s: 32B-swizzled K-major, 16 f16
+                        // per row per tile (every tile holds the same min codes: they
+                        // meet the hi and the lo halves of the activation sums)
+                        uint32_t w[8];
+                        min_words<KIND>(row, w);
+#pragma unroll
+                        for (int t = 0; t < MN::TILES; ++t) {
+                            uint8_t* tb = amin + t * MIN_TILE + (r >> 3) * 256 + (r & 7) * 32;
+                            const int sw = (r >> 2) & 1;
+                            *reinterpret_cast<uint4*>(tb + ((0 ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                            *reinterpret_cast<uint4*>(tb + ((1 ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                        }
+                        fence_proxy_async();
+                    }
+                }
+                if (ok) {
+                    tc_fence_after();
+                    tmem_st32(tmem + lane_addr + i * kACols2, o[0]);
+                    tmem_st32(tmem + lane_addr + i * kACols2 + kACols, o[1]);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[i]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[rs]);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - kEpi0;
+        const int quad = warp & 3;
+        const int half = ew >> 2;                  // column half: 64 columns each
+        const int r = quad * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        float2 acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
+        const Span span = cta_span(a);
+        const int nloc = span.n;
+        int et = span.t0, es = span.s0;
+        for (int s = 0; s < nloc;) {
+            const int seg_end = min(nloc, s + a.nsup - es);
+            const bool whole = es == 0 && seg_end - s == a.nsup;
+            for (; s < seg_end; ++s) {
+                const float* sc = sbuf + ((s & 1) * BM + r) * 8;
+                warp_wait_bar(&sc_full[s & 1], (s >> 1) & 1, abort_flag, a.err);
+                const int h = 2 * s + 1;
+                const bool ok = warp_wait_bar(&done[h % NS], (h / NS) & 1, abort_flag, a.err);
+                tc_fence_after();
+                const float2 d2 = make_float2(sc[0], sc[0]), ndm2 = make_float2(-sc[1], -sc[1]);
+                const uint32_t dcol = P::D1COL + (s & 1) * BN + half * 64;
+                if (ok) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float v[16];
+                        tmem_ld16(tmem + lane_addr + dcol + c * 16, v);
+                        if constexpr (MN::ON) {
+                            float w2[16];
+                            tmem_ld16(tmem + lane_addr + P::D2COL + half * 64 + c * 16, w2);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                acc[c * 8 + i] = __ffma2_rn(ndm2, make_float2(w2[2 * i], w2[2 * i + 1]),
+                                                            __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]),
+                                                                       acc[c * 8 + i]));
+                        } else {
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                acc[c * 8 + i] = __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]), acc[c * 8 + i]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(d_empty);
+                    mbar_arrive(&sc_empty[s & 1]);
+                }
+            }
+            if (!*abort_flag) store_tile(a, span, et, whole, half, r, acc);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
+            es = 0;
+            ++et;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// The kernel for a format and its dynamic shared memory: the super-block
+// pipeline for formats with one scale per 256 elements, the per-sub-step one
+// for the per-32 formats.
+using TcKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
+template <int KIND>
+TcKernel tc_kernel(int* smem_bytes) {
+    if constexpr (TcGeo<KIND>::PER32) {
+        *smem_bytes = Layout<KIND>::BYTES;
+        return k_gemm_tc<KIND>;
+    } else {
+        *smem_bytes = LayoutSB<KIND>::BYTES;
+        return k_gemm_sb<KIND>;
+    }
+}
+
 // Per-group activation sums for the min term: out[n][s][0..G) = hi, [G..2G) = lo
 // with hi = f16(sum), lo = f16(sum - hi); groups of 32 (Q4_K, Q5_K) or 16 (Q2_K).
 // One thread per group, reading its 16 or 32 halves with 16-byte loads (the
@@ -998,8 +1378,9 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
             return;
         }
     }
-    auto kern = k_gemm_tc<KIND>;
-    if ((*e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES)) != cudaSuccess) return;
+    int smem_bytes = 0;
+    const TcKernel kern = tc_kernel<KIND>(&smem_bytes);
+    if ((*e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess) return;
     TcArgs a;
     a.M = M;
     a.N = N;
@@ -1012,7 +1393,7 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     a.part = G ? reinterpret_cast<float*>(ws + xs_bytes) : nullptr;
     a.err = p.err;
     const dim3 grid = G ? dim3(G) : dim3(tiles_m, tiles_n);
-    kern<<<grid, kThreads, L::BYTES, s>>>(tmW, tmX, tmB, a);
+    kern<<<grid, kThreads, smem_bytes, s>>>(tmW, tmX, tmB, a);
     count_launch(1);
     if ((*e = cudaGetLastError()) != cudaSuccess || !G) return;
     cudaLaunchConfig_t cfg = {};
@@ -1105,8 +1486,9 @@ void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
             return;
         }
     }
-    auto kern = k_gemm_tc<KIND>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) != cudaSuccess) {
+    int smem_bytes = 0;
+    const TcKernel kern = tc_kernel<KIND>(&smem_bytes);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess) {
         *status = QMM_ERR_CUDA;
         return;
     }
@@ -1122,7 +1504,7 @@ void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
     a.part = nullptr;   // one tile per CTA: no partial-tile scratch
     a.err = p.err;
     const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);
-    kern<<<grid, kThreads, L::BYTES, s>>>(tmW, tmX, tmB, a);
+    kern<<<grid, kThreads, smem_bytes, s>>>(tmW, tmX, tmB, a);
     count_launch(1);
     if (cudaGetLastError() != cudaSuccess) *status = QMM_ERR_CUDA;
 }
