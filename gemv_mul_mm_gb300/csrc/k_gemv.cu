@@ -63,6 +63,7 @@
 #include "qmm.h"
 #include "qmm_internal.cuh"
 #include "sm100_async.cuh"
+#include "tc_fastdec.cuh"
 
 namespace qmm {
 namespace {
@@ -151,31 +152,6 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 // unit decoders: acc[n] += sum over the unit's elements of W * x[n]
 // ---------------------------------------------------------------------------
 
-// Any format, from shared bytes (scale applied per element).
-template <int KIND, int NC>
-__device__ __forceinline__ void unit_generic(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
-    constexpr int BB = Geo<KIND>::BB, BE = Geo<KIND>::BE, UB = SG<KIND>::UB;
-#pragma unroll 1
-    for (int blk = 0; blk < UB; ++blk) {
-        const uint8_t* b = u + blk * BB;
-#pragma unroll 1
-        for (int j = 0; j < BE / 32; ++j) {
-            const int kb = k0 + blk * BE + 32 * j;
-            float s[NC];
-#pragma unroll
-            for (int n = 0; n < NC; ++n) s[n] = 0.f;
-#pragma unroll 8
-            for (int i = 0; i < 32; ++i) {
-                const float v = elem32<KIND>(b, j, i);
-#pragma unroll
-                for (int n = 0; n < NC; ++n) s[n] = fmaf(v, xs[n * K + kb + i], s[n]);
-            }
-#pragma unroll
-            for (int n = 0; n < NC; ++n) acc[n] += s[n];
-        }
-    }
-}
-
 // Q4_0 staged-activation order. The decoder walks four 32-bit words of code
 // bytes per block. Odd blocks start 4-byte aligned at their codes (word j =
 // code bytes 4j..4j+3); even blocks start 2 bytes off, so their word 0 is
@@ -207,6 +183,17 @@ __host__ __device__ __forceinline__ int q4_slot(int e, bool even) {
 __host__ __device__ __forceinline__ int q4_pow(int i) {
     return (i <= 4) ? 4 * i - 16 : 4 * (i - 3) - 16;
 }
+
+// Formats whose minimum term needs the activation sums of each 16-element group.
+template <int KIND> struct XSum { static constexpr bool ON = KIND == Q4_K || KIND == Q5_K || KIND == Q2_K; };
+
+// Codebook formats (IQ4_NL, IQ4_XS, MXFP4) stage the activations of each
+// 32-element group in the order their decoder meets the elements: a code word
+// holds elements 4w .. 4w + 3 in its low nibbles and 16 + 4w .. in its high
+// nibbles, and the register table lookup returns them interleaved, element
+// 16 h + 4 w + j at slot 8 w + 2 j + h.
+__host__ __device__ __forceinline__ int cb_slot(int e) { return 8 * ((e >> 2) & 3) + 2 * (e & 3) + (e >> 4); }
+template <int KIND> struct CbOrder { static constexpr bool ON = KIND == IQ4_NL || KIND == IQ4_XS || KIND == MXFP4; };
 
 // Q4_0, one activation column: 8 blocks of 18 bytes (144 B, 16-byte aligned
 // in shared memory), fully unrolled (the fastest form for a single column).
@@ -406,8 +393,333 @@ __device__ __forceinline__ void unit_q8_0(const uint8_t* u, const float* xs, int
     }
 }
 
+// ---------------------------------------------------------------------------
+// Byte-code decoders for the other formats. A word of four code bytes c_k
+// (unsigned, biased) becomes four exact fp32 values: byte k placed under the
+// exponent of 2^23 (one byte permute) reads 2^23 + c_k, and one packed
+// subtract of 2^23 + bias leaves c_k - bias exactly. Packed FMAs then add
+// (c_k - bias) * x_k into per-group partial sums, which the group's fp32 scale
+// multiplies afterwards (the minimum term of Q4_K / Q5_K / Q2_K multiplies
+// the group's activation sum). Codebooks are looked up four nibbles at a time
+// in registers (byte permutes, see lut16), never in memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 nbias(float bias) { return make_float2(-(8388608.f + bias), -(8388608.f + bias)); }
+
+// s[n] += sum_k (byte k of w + nb) * x[n * K + k], k = 0..3 (x 16-byte aligned)
+template <int NC>
+__device__ __forceinline__ void dot4(uint32_t w, float2 nb, const float* x, int K, float2 (&s)[NC]) {
+    const float2 q01 = __fadd2_rn(make_float2(__uint_as_float(prmt(w, 0x4B000000u, 0x7540u)),
+                                              __uint_as_float(prmt(w, 0x4B000000u, 0x7541u))), nb);
+    const float2 q23 = __fadd2_rn(make_float2(__uint_as_float(prmt(w, 0x4B000000u, 0x7542u)),
+                                              __uint_as_float(prmt(w, 0x4B000000u, 0x7543u))), nb);
+#pragma unroll
+    for (int n = 0; n < NC; ++n) {
+        const float4 xv = *reinterpret_cast<const float4*>(x + n * K);
+        s[n] = __ffma2_rn(q01, make_float2(xv.x, xv.y), s[n]);
+        s[n] = __ffma2_rn(q23, make_float2(xv.z, xv.w), s[n]);
+    }
+}
+
+template <int NC>
+__device__ __forceinline__ void zero2(float2 (&s)[NC]) {
+#pragma unroll
+    for (int n = 0; n < NC; ++n) s[n] = make_float2(0.f, 0.f);
+}
+
+// the four bits v (bits 0..3) moved to bit 4 of bytes 0..3
+__device__ __forceinline__ uint32_t bit4_to_bytes(uint32_t v) { return ((v * 0x00204081u) & 0x01010101u) << 4; }
+
+// Q5_0: pairs of 22-byte blocks (44 bytes, 4-byte aligned in the unit).
+template <int NC>
+__device__ __forceinline__ void unit_q5_0(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+    const float2 nb = nbias(16.f);
+#pragma unroll 1
+    for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(u + 44 * pr);
+        uint32_t w[11];
+#pragma unroll
+        for (int i = 0; i < 11; ++i) w[i] = pw[i];
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            // block 2pr: d at bytes 0-1, qh 2-5, codes 6-21; block 2pr + 1: d 22-23, qh 24-27, codes 28-43
+            const float d = h2f(hb ? (w[5] >> 16) : w[0]);
+            const uint32_t qh = hb ? w[6] : __funnelshift_r(w[0], w[1], 16);
+            const int kb = k0 + 32 * (2 * pr + hb);
+            float2 S[NC];
+            zero2(S);
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+                const uint32_t q = hb ? w[7 + wi] : __funnelshift_r(w[1 + wi], w[2 + wi], 16);
+                const uint32_t lo = (q & 0x0F0F0F0Fu) | bit4_to_bytes((qh >> (4 * wi)) & 0xFu);
+                const uint32_t hi = ((q >> 4) & 0x0F0F0F0Fu) | bit4_to_bytes((qh >> (16 + 4 * wi)) & 0xFu);
+                dot4<NC>(lo, nb, xs + kb + 4 * wi, K, S);
+                dot4<NC>(hi, nb, xs + kb + 16 + 4 * wi, K, S);
+            }
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[n] = fmaf(d, S[n].x + S[n].y, acc[n]);
+        }
+    }
+}
+
+// One 32-element codebook group from its four code words (activations in
+// codebook order, see cb_slot); table T biased by +128.
+template <typename T, int NC>
+__device__ __forceinline__ void cb_group(const uint32_t (&q)[4], const float* x, int K, float2 (&S)[NC]) {
+    const float2 nb = nbias(128.f);
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+        dot4<NC>(lut16<T>(q[wi]), nb, x + 8 * wi, K, S);
+        dot4<NC>(lut16<T>(q[wi] >> 16), nb, x + 8 * wi + 4, K, S);
+    }
+}
+
+// IQ4_NL: pairs of 18-byte blocks, as Q4_0.
+template <int NC>
+__device__ __forceinline__ void unit_iq4nl(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+#pragma unroll 1
+    for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(u + 36 * pr);
+        uint32_t w[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) w[i] = pw[i];
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            const float d = h2f(hb ? (w[4] >> 16) : w[0]);
+            uint32_t q[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q[i] = hb ? w[5 + i] : __funnelshift_r(w[i], w[i + 1], 16);
+            float2 S[NC];
+            zero2(S);
+            cb_group<KvTable, NC>(q, xs + k0 + 32 * (2 * pr + hb), K, S);
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[n] = fmaf(d, S[n].x + S[n].y, acc[n]);
+        }
+    }
+}
+
+// MXFP4: groups of four 17-byte blocks (68 bytes, 4-byte aligned in the unit).
+template <int NC>
+__device__ __forceinline__ void unit_mxfp4(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+#pragma unroll 1
+    for (int gq = 0; gq < 4; ++gq) {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(u + 68 * gq);
+        uint32_t w[17];
+#pragma unroll
+        for (int i = 0; i < 17; ++i) w[i] = pw[i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // block j: exponent byte 17 j, codes 17 j + 1 .. 17 j + 16
+            const int bo = 17 * j, wo = (bo + 1) >> 2, sh = ((bo + 1) & 3) * 8;
+            const uint32_t e = (w[bo >> 2] >> ((bo & 3) * 8)) & 0xFFu;
+            uint32_t q[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q[i] = sh ? __funnelshift_r(w[wo + i], w[wo + i + 1], sh) : w[wo + i];
+            float2 S[NC];
+            zero2(S);
+            cb_group<E2m1Table, NC>(q, xs + k0 + 32 * (4 * gq + j), K, S);
+            const float sc = e8m0f(e);
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[n] = fmaf(sc, S[n].x + S[n].y, acc[n]);
+        }
+    }
+}
+
+// Q4_K / Q5_K (6-bit scale and min of sub-block j from the 12-byte field,
+// held as three words s0 = bytes 0-3, s1 = 4-7, s2 = 8-11).
+__device__ __forceinline__ void k4_sm_words(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc, int& mn) {
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63;
+        mn = (s1 >> (8 * j)) & 63;
+    } else {
+        const int b = 8 * (j - 4);
+        sc = ((s2 >> b) & 15) | (((s0 >> b) >> 6 & 3) << 4);
+        mn = ((s2 >> b) >> 4 & 15) | (((s1 >> b) >> 6 & 3) << 4);
+    }
+}
+
+// Q4_K (144 B, 16-byte aligned) and Q5_K (176 B, 16-byte aligned): one
+// super-block per unit, 64 elements (sub-blocks 2c and 2c + 1) per step.
 template <int KIND, int NC>
-__device__ __forceinline__ void unit(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+__device__ __forceinline__ void unit_k45(const uint8_t* u, const float* xs, const float* xsum, int K, int k0,
+                                         float (&acc)[NC]) {
+    const uint4 h = *reinterpret_cast<const uint4*>(u);
+    const float d = h2f(h.x), dmin = h2f(h.x >> 16);
+    uint32_t qh[8];
+    if constexpr (KIND == Q5_K) {
+        const uint4 a = *reinterpret_cast<const uint4*>(u + 16), b = *reinterpret_cast<const uint4*>(u + 32);
+        qh[0] = a.x; qh[1] = a.y; qh[2] = a.z; qh[3] = a.w;
+        qh[4] = b.x; qh[5] = b.y; qh[6] = b.z; qh[7] = b.w;
+    }
+    constexpr int QS = (KIND == Q4_K) ? 16 : 48;
+    const float2 nb = nbias(0.f);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(u + QS + 32 * c);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(u + QS + 32 * c + 16);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float2 S0[NC], S1[NC];
+        zero2(S0);
+        zero2(S1);
+        const int kb = k0 + 64 * c;
+#pragma unroll
+        for (int wi = 0; wi < 8; ++wi) {
+            uint32_t lo = w[wi] & 0x0F0F0F0Fu, hi = (w[wi] >> 4) & 0x0F0F0F0Fu;
+            if constexpr (KIND == Q5_K) {
+                lo |= ((qh[wi] >> (2 * c)) & 0x01010101u) << 4;
+                hi |= ((qh[wi] >> (2 * c + 1)) & 0x01010101u) << 4;
+            }
+            dot4<NC>(lo, nb, xs + kb + 4 * wi, K, S0);
+            dot4<NC>(hi, nb, xs + kb + 32 + 4 * wi, K, S1);
+        }
+        int sc0, m0, sc1, m1;
+        k4_sm_words(h.y, h.z, h.w, 2 * c, sc0, m0);
+        k4_sm_words(h.y, h.z, h.w, 2 * c + 1, sc1, m1);
+        const float a0 = d * static_cast<float>(sc0), b0 = dmin * static_cast<float>(m0);
+        const float a1 = d * static_cast<float>(sc1), b1 = dmin * static_cast<float>(m1);
+        const int g = kb >> 4;   // first 16-element group of sub-block 2c
+#pragma unroll
+        for (int n = 0; n < NC; ++n) {
+            const float* xsn = xsum + n * (K >> 4) + g;
+            float t = fmaf(a0, S0[n].x + S0[n].y, acc[n]);
+            t = fmaf(-b0, xsn[0] + xsn[1], t);
+            t = fmaf(a1, S1[n].x + S1[n].y, t);
+            acc[n] = fmaf(-b1, xsn[2] + xsn[3], t);
+        }
+    }
+}
+
+// Q6_K (210 B, 2-byte aligned): per 128-element half h and low-nibble run p,
+// 32 code bytes and the shared 32 bytes of high bits; int8 scale per 16.
+template <int NC>
+__device__ __forceinline__ void unit_q6k(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+    const float d = h2f(ld16(u, 208));
+    const float2 nb = nbias(32.f);
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        uint32_t qw[8];
+        ld_words<8, 2>(u + 128 + 32 * h, qw);
+#pragma unroll 1
+        for (int p = 0; p < 2; ++p) {
+            uint32_t w[8];
+            ld_words<8, 2>(u + 64 * h + 32 * p, w);
+            float2 SL[2][NC], SH[2][NC];   // [16-element half of the run][column]
+            zero2(SL[0]);
+            zero2(SL[1]);
+            zero2(SH[0]);
+            zero2(SH[1]);
+            const int kl = k0 + 128 * h + 32 * p, kh = kl + 64;   // groups g = p and g = p + 2
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) {
+                const uint32_t lo = (w[wi] & 0x0F0F0F0Fu) | (((qw[wi] >> (2 * p)) << 4) & 0x30303030u);
+                const uint32_t hi = ((w[wi] >> 4) & 0x0F0F0F0Fu) | (((qw[wi] >> (2 * p + 4)) << 4) & 0x30303030u);
+                dot4<NC>(lo, nb, xs + kl + 4 * wi, K, SL[wi >> 2]);
+                dot4<NC>(hi, nb, xs + kh + 4 * wi, K, SH[wi >> 2]);
+            }
+            // scale index (element / 16): 8 h + 2 g + (l >= 16)
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const float sl = d * static_cast<float>(static_cast<int8_t>(u[192 + 8 * h + 2 * p + t]));
+                const float shh = d * static_cast<float>(static_cast<int8_t>(u[192 + 8 * h + 2 * (p + 2) + t]));
+#pragma unroll
+                for (int n = 0; n < NC; ++n)
+                    acc[n] = fmaf(shh, SH[t][n].x + SH[t][n].y, fmaf(sl, SL[t][n].x + SL[t][n].y, acc[n]));
+            }
+        }
+    }
+}
+
+// Q2_K (84 B, 4-byte aligned): 2-bit codes, 4-bit scale and min per 16.
+template <int NC>
+__device__ __forceinline__ void unit_q2k(const uint8_t* u, const float* xs, const float* xsum, int K, int k0,
+                                         float (&acc)[NC]) {
+    const uint32_t dd = *reinterpret_cast<const uint32_t*>(u + 80);
+    const float d = h2f(dd), dmin = h2f(dd >> 16);
+    const float2 nb = nbias(0.f);
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = reinterpret_cast<const uint32_t*>(u + 16 + 32 * h)[i];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float2 S[2][NC];
+            zero2(S[0]);
+            zero2(S[1]);
+            const int kb = k0 + 128 * h + 32 * g;
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) dot4<NC>((w[wi] >> (2 * g)) & 0x03030303u, nb, xs + kb + 4 * wi, K, S[wi >> 2]);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int idx = 8 * h + 2 * g + t;
+                const uint32_t sb = u[idx];
+                const float a = d * static_cast<float>(sb & 15), b = dmin * static_cast<float>(sb >> 4);
+#pragma unroll
+                for (int n = 0; n < NC; ++n)
+                    acc[n] = fmaf(-b, xsum[n * (K >> 4) + ((kb >> 4) + t)], fmaf(a, S[t][n].x + S[t][n].y, acc[n]));
+            }
+        }
+    }
+}
+
+// Q3_K (110 B, 2-byte aligned): 2-bit codes plus the hmask bit (clear = -4),
+// 6-bit scale minus 32 per 16.
+template <int NC>
+__device__ __forceinline__ void unit_q3k(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+    const float d = h2f(ld16(u, 108));
+    const float2 nb = nbias(4.f);
+    uint32_t hm[8];
+    ld_words<8, 2>(u, hm);
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        uint32_t w[8];
+        ld_words<8, 2>(u + 32 + 32 * h, w);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int j = 4 * h + g;
+            float2 S[2][NC];
+            zero2(S[0]);
+            zero2(S[1]);
+            const int kb = k0 + 128 * h + 32 * g;
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) {
+                const uint32_t c = ((w[wi] >> (2 * g)) & 0x03030303u) | (((hm[wi] >> j) & 0x01010101u) << 2);
+                dot4<NC>(c, nb, xs + kb + 4 * wi, K, S[wi >> 2]);
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const float a = d * static_cast<float>(q3_scale(u + 96, 2 * j + t) - 32);
+#pragma unroll
+                for (int n = 0; n < NC; ++n) acc[n] = fmaf(a, S[t][n].x + S[t][n].y, acc[n]);
+            }
+        }
+    }
+}
+
+// IQ4_XS (136 B, 8-byte aligned): eight 32-element codebook groups, 6-bit
+// group scale minus 32.
+template <int NC>
+__device__ __forceinline__ void unit_iq4xs(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+    const uint2 hd = *reinterpret_cast<const uint2*>(u);
+    const float d = h2f(hd.x);
+    const uint32_t sh = hd.x >> 16, sl = hd.y;
+#pragma unroll 1
+    for (int ib = 0; ib < 8; ++ib) {
+        const uint2 c0 = *reinterpret_cast<const uint2*>(u + 8 + 16 * ib);
+        const uint2 c1 = *reinterpret_cast<const uint2*>(u + 16 + 16 * ib);
+        const uint32_t q[4] = {c0.x, c0.y, c1.x, c1.y};
+        float2 S[NC];
+        zero2(S);
+        cb_group<KvTable, NC>(q, xs + k0 + 32 * ib, K, S);
+        const int ls = static_cast<int>(((sl >> (4 * ib)) & 15u) | (((sh >> (2 * ib)) & 3u) << 4));
+        const float a = d * static_cast<float>(ls - 32);
+#pragma unroll
+        for (int n = 0; n < NC; ++n) acc[n] = fmaf(a, S[n].x + S[n].y, acc[n]);
+    }
+}
+
+template <int KIND, int NC>
+__device__ __forceinline__ void unit(const uint8_t* u, const float* xs, const float* xsum, int K, int k0,
+                                     float (&acc)[NC]) {
     if constexpr (KIND == Q4_0) {
         static_assert(SG<KIND>::UB == 8, "the Q4_0 decoder takes eight blocks");
         if constexpr (NC == 1) unit_q4_0_flat<NC>(u, xs, K, k0, acc);
@@ -415,8 +727,26 @@ __device__ __forceinline__ void unit(const uint8_t* u, const float* xs, int K, i
     } else if constexpr (KIND == Q8_0) {
         static_assert(SG<KIND>::UB == 8, "the Q8_0 decoder takes eight blocks");
         unit_q8_0<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == Q5_0) {
+        static_assert(SG<KIND>::UB == 8, "the Q5_0 decoder takes eight blocks");
+        unit_q5_0<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == IQ4_NL) {
+        static_assert(SG<KIND>::UB == 8, "the IQ4_NL decoder takes eight blocks");
+        unit_iq4nl<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == MXFP4) {
+        static_assert(SG<KIND>::UB == 16, "the MXFP4 decoder takes sixteen blocks");
+        unit_mxfp4<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == Q4_K || KIND == Q5_K) {
+        unit_k45<KIND, NC>(u, xs, xsum, K, k0, acc);
+    } else if constexpr (KIND == Q6_K) {
+        unit_q6k<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == Q2_K) {
+        unit_q2k<NC>(u, xs, xsum, K, k0, acc);
+    } else if constexpr (KIND == Q3_K) {
+        unit_q3k<NC>(u, xs, K, k0, acc);
     } else {
-        unit_generic<KIND, NC>(u, xs, K, k0, acc);
+        static_assert(KIND == IQ4_XS, "every format has a unit decoder");
+        unit_iq4xs<NC>(u, xs, K, k0, acc);
     }
 }
 
@@ -432,11 +762,12 @@ struct Lay {
 __host__ __device__ __forceinline__ int tbl_ints(int E, int A) { return 3 * (E + 2) + 2 * A + 4; }
 
 __host__ __device__ __forceinline__ Lay layout(int stage_b, int stages, int ncmax, int K, int nw, bool grouped, int E,
-                                               int A) {
+                                               int A, bool xsum) {
     Lay l;
     int off = stages * stage_b;
     l.xs = off;
     off += ncmax * K * 4;
+    off += xsum ? ncmax * (K / 16) * 4 : 0;   // per-16 activation sums (formats with mins)
     l.red = off;
     off += 2 * ncmax * nw * 32 * 4;
     l.tbl = off;
@@ -628,10 +959,41 @@ __device__ void stage_x(const GemvArgs& a, const Tables& t, const Item& it, floa
                     // times 2^-p, an exact power-of-two product
                     xs[n * K + 32 * b + slot] = vv[c] * __int_as_float((127 - q4_pow(slot & 7)) << 23);
                 }
+            } else if constexpr (CbOrder<KIND>::ON) {
+                // MXFP4's table holds twice the E2M1 value: its activations are
+                // staged halved (exact)
+                const float sc = (KIND == MXFP4) ? 0.5f : 1.f;
+                const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int kk = k + c;
+                    xs[n * K + (kk & ~31) + cb_slot(kk & 31)] = vv[c] * sc;
+                }
             } else {
                 *reinterpret_cast<float4*>(xs + n * K + k) = v[j];
             }
         }
+    }
+}
+
+// Per-16 activation sums (sequential fp32 adds over the staged values, in
+// natural order) for the formats with a minimum term: xsum[n * K / 16 + g].
+template <int NCMAX>
+__device__ void stage_xsum(const float* xs, float* xsum, int K, int tid, int nthr) {
+    const int per = K / 16;
+    for (int i = tid; i < NCMAX * per; i += nthr) {
+        const int n = i / per, g = i - n * per;
+        const float4* p = reinterpret_cast<const float4*>(xs + n * K + 16 * g);
+        float t = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v = p[q];
+            t += v.x;
+            t += v.y;
+            t += v.z;
+            t += v.w;
+        }
+        xsum[i] = t;
     }
 }
 
@@ -655,7 +1017,7 @@ __device__ __forceinline__ void consume_item(const GemvArgs& a, const Tables& t,
         const bool ok = !*abort_flag && mbar_wait(&full[s], use & 1, abort_flag, a.err);
         const int units = min(nwu, a.upr - c * nwu);
         if (ok && u < units)
-            unit<KIND, NC>(stage0 + s * stage_b + lane * a.stride + u * G::UNIT_B, xs, K,
+            unit<KIND, NC>(stage0 + s * stage_b + lane * a.stride + u * G::UNIT_B, xs, xs + NCMAX * K, K,
                            (c * nwu + u) * G::UNIT_E, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -706,7 +1068,7 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32, MinBlocks<KIND>::V)
     const bool grouped = a.x_row != nullptr;
     const int K = a.K;
     const int stage_b = kRows * a.stride;
-    const Lay L = layout(stage_b, a.stages, NCMAX, K, NW, grouped, a.n_experts, a.n_assign);
+    const Lay L = layout(stage_b, a.stages, NCMAX, K, NW, grouped, a.n_experts, a.n_assign, XSum<KIND>::ON);
     uint8_t* stage0 = smem;
     float* xs = reinterpret_cast<float*>(smem + L.xs);
     float* red = reinterpret_cast<float*>(smem + L.red);
@@ -836,6 +1198,10 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32, MinBlocks<KIND>::V)
             if (cur_e >= 0) named_bar_sync(1, NW * 32);   // everyone is done with the old activations
             stage_x<KIND, NCMAX>(a, T, item, xs, threadIdx.x, NW * 32);
             named_bar_sync(1, NW * 32);
+            if constexpr (XSum<KIND>::ON) {
+                stage_xsum<NCMAX>(xs, xs + NCMAX * K, K, threadIdx.x, NW * 32);
+                named_bar_sync(1, NW * 32);
+            }
             cur_e = item.e;
             cur_c = item.col0;
         }
@@ -926,7 +1292,9 @@ Plan plan(const Problem& p) {
         if (2 * bg > 256) continue;                 // TMA box dimension limit (256 8-byte words)
         const int stride = bg * 16;
         const int stage_b = kRows * stride;
-        auto total = [&](int st) { return layout(stage_b, st, pl.ncmax, K, G::NW, grouped, E, A).total; };
+        auto total = [&](int st) {
+            return layout(stage_b, st, pl.ncmax, K, G::NW, grouped, E, A, XSum<KIND>::ON).total;
+        };
         if (ngroups > kMaxStages || total(ngroups) > kSmemBudget) continue;
         // two CTAs per SM when the stages fit in half the SM, else one deep CTA
         const int want = ngroups >= 4 ? ngroups : 4;
