@@ -199,12 +199,14 @@ int qdequant(int kind, const void* blocks, size_t blocks_bytes, int64_t rows, in
 int qgemm_ex(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype, size_t x_elems,
              float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, uint32_t flags, void* stream) {
     if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
-    if (flags & ~static_cast<uint32_t>(QMM_FLAG_WEIGHTS_CONST)) return QMM_ERR_BAD_ARGUMENT;
+    constexpr uint32_t kKnown = QMM_FLAG_WEIGHTS_CONST | QMM_FLAG_Y_F16 | QMM_FLAG_Y_BF16;
+    if ((flags & ~kKnown) || ((flags & QMM_FLAG_Y_F16) && (flags & QMM_FLAG_Y_BF16))) return QMM_ERR_BAD_ARGUMENT;
+    const int y_dtype = (flags & QMM_FLAG_Y_F16) ? 1 : (flags & QMM_FLAG_Y_BF16) ? 2 : 0;
     if (M < 0 || K < 0 || N < 0) return QMM_ERR_BAD_ARGUMENT;
     if (M == 0 || K == 0 || N == 0) return QMM_ERR_EMPTY_SHAPE;
     if (!W || !X || !Y) return QMM_ERR_NULL_POINTER;
     if (int r = check_x(X, x_dtype)) return r;
-    if (reinterpret_cast<uintptr_t>(Y) % 4) return QMM_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(Y) % y_size(y_dtype)) return QMM_ERR_MISALIGNED;
     if (K % kKinds[kind].block_elems) return QMM_ERR_COLS_NOT_BLOCK_ALIGNED;
     const size_t rb = qmm_row_bytes(kind, K);
     if (w_bytes / rb < static_cast<size_t>(M)) return QMM_ERR_WEIGHTS_TOO_SMALL;
@@ -214,6 +216,7 @@ int qgemm_ex(int kind, const void* W, size_t w_bytes, const void* X, int x_dtype
     if (int r = err_ptr(&err)) return r;
 
     Problem p;
+    p.y_dtype = y_dtype;
     p.kind = kind;
     p.W = static_cast<const uint8_t*>(W);
     p.row_bytes = rb;
@@ -325,7 +328,7 @@ int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X, int x_
     p.x_dtype = x_dtype;
     p.Y = Y;
     p.err = err;
-    if (!gemm_tc_ok(p)) return QMM_ERR_UNIMPLEMENTED;
+    if (x_dtype != QMM_F16 || !gemm_tc_ok(p)) return QMM_ERR_UNIMPLEMENTED;
     const int r = launch_gemm_tc_noalloc(p, static_cast<cudaStream_t>(stream));
     if (r == QMM_OK) t_last_path = 3;
     return r;

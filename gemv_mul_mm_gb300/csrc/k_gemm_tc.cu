@@ -111,10 +111,17 @@ template <int KIND> struct Mins {
 };
 
 struct TcArgs {
-    int M, N, K, nsup;
+    int M, N, K, nsup;   // N: activation rows the MMAs see (2 per token in pair mode)
     int tiles_m;      // tiles along M; tile t is (t % tiles_m, t / tiles_m)
     int wq, wr;       // shared super-steps: work = tiles * nsup = wq * G + wr (work < 2^31)
     float* Y;
+    int y_dtype;      // 0 fp32, 1 f16, 2 bf16
+    // pair mode (fp32 activations): activation rows 2n and 2n + 1 are the f16
+    // high and low parts of token n scaled by 2^s_n; Y[n] = (column 2n +
+    // column 2n + 1) * inv_scale[n]. Only with one tile per CTA.
+    int pair;
+    int ntok;
+    const float* inv_scale;
     float* part;      // shared tiles: [CTA][2][BN][BM] fp32 partial tiles, or null (one tile per CTA)
     unsigned* err;
 };
@@ -151,7 +158,26 @@ __device__ __forceinline__ void store_tile(const TcArgs& a, const Span& sp, int 
         const int m0 = sp.t0 < 0 ? static_cast<int>(blockIdx.x) * BM : (t % a.tiles_m) * BM;
         const int n0 = (sp.t0 < 0 ? static_cast<int>(blockIdx.y) : t / a.tiles_m) * BN + half * 64;
         const int m = m0 + r;
+        if (a.pair) {
+            // columns 2i, 2i + 1 of this thread are the two parts of token n0 / 2 + i
+            const int tok0 = n0 >> 1;
+            const int tl = m < a.M ? min(32, a.ntok - tok0) : 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < tl)
+                    store_y(a.Y, a.y_dtype, static_cast<int64_t>(tok0 + i) * a.M + m,
+                            (acc[i].x + acc[i].y) * a.inv_scale[tok0 + i]);
+            return;
+        }
         lim = m < a.M ? min(64, a.N - n0) : 0;
+        if (a.y_dtype != 0) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                if (i < lim)
+                    store_y(a.Y, a.y_dtype, static_cast<int64_t>(n0 + i) * a.M + m,
+                            (i & 1) ? acc[i >> 1].y : acc[i >> 1].x);
+            return;
+        }
         dst = a.Y + static_cast<int64_t>(n0) * a.M + m;
         stride = a.M;
     } else {
@@ -1211,7 +1237,7 @@ constexpr int kFixThreads = 256;
 constexpr int kFixSplit = BM * BN / 4 / kFixThreads;
 __global__ void __launch_bounds__(kFixThreads) k_tile_fixup(const float* __restrict__ part, float* __restrict__ Y,
                                                             int M, int N, int tiles_m, int nsup, int64_t work,
-                                                            int G) {
+                                                            int G, int y_dtype) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int t = blockIdx.x;
     // CTA b covers steps [b * work / G, (b + 1) * work / G): step g lies in CTA ((g + 1) * G - 1) / work
@@ -1234,11 +1260,51 @@ __global__ void __launch_bounds__(kFixThreads) k_tile_fixup(const float* __restr
         v.z += u.z;
         v.w += u.w;
     }
-    float* y = Y + static_cast<int64_t>(n) * M + m0;
     const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        if (m0 + i < M) y[i] = vv[i];
+        if (m0 + i < M) store_y(Y, y_dtype, static_cast<int64_t>(n) * M + m0 + i, vv[i]);
+}
+
+// fp32 activations for the tensor cores: token row n, scaled by the power of
+// two 2^s_n that puts its largest magnitude in [2^9, 2^10), is split into
+// f16 parts hi = f16(x 2^s_n) and lo = f16(x 2^s_n - hi), written as rows
+// 2n and 2n + 1 of X2; inv_scale[n] = 2^-s_n. hi + lo equals x 2^s_n to about
+// 2^-22 relative, far inside the 1e-3 bar. The scale keeps every finite fp32
+// row inside f16's range, with room for the 32-element activation sums of
+// the min term (< 2^15), which are carried in f16 too. One CTA per token row.
+constexpr int kSplitThreads = 256;
+__global__ void __launch_bounds__(kSplitThreads) k_xsplit(const float* __restrict__ X, int K,
+                                                          __half* __restrict__ X2, float* __restrict__ inv_scale) {
+    __shared__ float red[kSplitThreads / 32];
+    const int64_t n = blockIdx.x;
+    const float* x = X + n * K;
+    float mx = 0.f;
+    for (int k = threadIdx.x; k < K; k += kSplitThreads) mx = fmaxf(mx, fabsf(x[k]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int i = 1; i < kSplitThreads / 32; ++i) mx = fmaxf(mx, red[i]);
+    // exponent of the largest magnitude (subnormal or zero rows count as 2^-127;
+    // a non-finite row keeps scale 1 and stays non-finite)
+    int se = 0;
+    if (mx < INFINITY) {
+        const int e = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
+        se = min(126, max(-126, 9 - e));
+    }
+    const float sc = __uint_as_float(static_cast<uint32_t>(se + 127) << 23);
+    if (threadIdx.x == 0) inv_scale[n] = __uint_as_float(static_cast<uint32_t>(127 - se) << 23);
+    __half* hi = X2 + (2 * n) * K;
+    __half* lo = hi + K;
+    for (int k = threadIdx.x; k < K; k += kSplitThreads) {
+        const float v = x[k] * sc;
+        const __half h = __float2half_rn(v);
+        hi[k] = h;
+        lo[k] = __float2half_rn(v - __half2float(h));
+    }
 }
 
 // ------------------------------------------------------------ host side
@@ -1300,9 +1366,11 @@ bool release_workspaces() {
 template <int KIND>
 void ok_kind(const Problem& p, bool* out) {
     // one CTA per tile puts the token tiles on grid.y (at most 65535 of them)
-    *out = !p.x_row && p.x_dtype == 1 && p.K % KSUP == 0 && p.row_bytes % 16 == 0 &&
-           reinterpret_cast<uintptr_t>(p.W) % 16 == 0 && reinterpret_cast<uintptr_t>(p.X) % 16 == 0 &&
-           p.M <= (int64_t(1) << 30) && (p.N + BN - 1) / BN <= 65535 && p.K <= (int64_t(1) << 30);
+    // fp32 activations run as two f16 rows per token (pair mode)
+    const int64_t rows = p.x_dtype == 1 ? p.N : 2 * p.N;
+    const bool x_ok = p.x_dtype == 1 ? reinterpret_cast<uintptr_t>(p.X) % 16 == 0 : p.x_dtype == 0;
+    *out = !p.x_row && x_ok && p.K % KSUP == 0 && p.row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(p.W) % 16 == 0 &&
+           p.M <= (int64_t(1) << 30) && (rows + BN - 1) / BN <= 65535 && p.K <= (int64_t(1) << 30);
 }
 
 // QMM_TC_SPLIT: 0 = automatic, 1 = one tile per CTA always, 2 = shared
@@ -1335,30 +1403,48 @@ template <int KIND>
 void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     using R = Raw<KIND>;
     using MN = Mins<KIND>;
-    using L = Layout<KIND>;
-    const int M = static_cast<int>(p.M), N = static_cast<int>(p.N), K = static_cast<int>(p.K);
+    const int M = static_cast<int>(p.M), K = static_cast<int>(p.K);
+    const int ntok = static_cast<int>(p.N);
+    // fp32 activations run as f16 (hi, lo) pairs: two MMA rows per token
+    const bool pair = p.x_dtype == 0;
+    const int N = pair ? 2 * ntok : ntok;
     const int nsup = K / KSUP;
     const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
     const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
     int dev = 0;
     if ((*e = cudaGetDevice(&dev)) != cudaSuccess) return;
-    const int G = split_grid(tiles, nsup, sm_count(dev));
-    // one workspace: the activation sums (formats with mins), then the partial tiles
+    const int G = pair ? 0 : split_grid(tiles, nsup, sm_count(dev));
+    // one workspace: the (hi, lo) activations and their scales (fp32 input),
+    // the activation sums (formats with mins), then the partial tiles
+    const size_t x2_bytes = pair ? ((static_cast<size_t>(N) * K * 2 + 255) & ~size_t(255)) : 0;
+    const size_t inv_bytes = pair ? ((static_cast<size_t>(ntok) * 4 + 255) & ~size_t(255)) : 0;
     const size_t xs_bytes = MN::ON ? ((static_cast<size_t>(N) * nsup * MN::KMW * 2 + 255) & ~size_t(255)) : 0;
     const size_t part_bytes = static_cast<size_t>(G) * 2 * BM * BN * sizeof(float);
     uint8_t* ws = nullptr;
-    if (xs_bytes + part_bytes) {
+    if (x2_bytes + inv_bytes + xs_bytes + part_bytes) {
         bool capturing = false;
-        ws = static_cast<uint8_t*>(workspace(xs_bytes + part_bytes, s, &capturing));
+        ws = static_cast<uint8_t*>(workspace(x2_bytes + inv_bytes + xs_bytes + part_bytes, s, &capturing));
         if (!ws) {
             *e = capturing ? cudaErrorStreamCaptureUnsupported : cudaErrorMemoryAllocation;
             return;
         }
     }
+    const __half* X = static_cast<const __half*>(p.X);
+    float* inv_scale = nullptr;
+    if (pair) {
+        __half* X2 = reinterpret_cast<__half*>(ws);
+        inv_scale = reinterpret_cast<float*>(ws + x2_bytes);
+        k_xsplit<<<static_cast<unsigned>(ntok), kSplitThreads, 0, s>>>(static_cast<const float*>(p.X), K, X2,
+                                                                          inv_scale);
+        count_launch(1);
+        if ((*e = cudaGetLastError()) != cudaSuccess) return;
+        X = X2;
+    }
+    uint8_t* xs_ws = ws ? ws + x2_bytes + inv_bytes : nullptr;
     CUtensorMap tmW, tmX, tmB;
     if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.W, p.row_bytes / 2, M, p.row_bytes, R::BOXB / 2, BM,
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.X, K, N, static_cast<uint64_t>(K) * 2, KSUB, BN,
+        !make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, K, N, static_cast<uint64_t>(K) * 2, KSUB, BN,
                   CU_TENSOR_MAP_SWIZZLE_128B)) {
         *e = cudaErrorInvalidValue;
         return;
@@ -1368,11 +1454,10 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
         const int threads = 256;
         const int64_t total = static_cast<int64_t>(N) * (K / (KSUP / MN::G));
         const int blocks = static_cast<int>(imin64((total + threads - 1) / threads, 4096));
-        k_xsums<<<blocks, threads, 0, s>>>(static_cast<const __half*>(p.X), N, K, KSUP / MN::G, MN::G,
-                                           reinterpret_cast<__half*>(ws));
+        k_xsums<<<blocks, threads, 0, s>>>(X, N, K, KSUP / MN::G, MN::G, reinterpret_cast<__half*>(xs_ws));
         count_launch(1);
         if ((*e = cudaGetLastError()) != cudaSuccess) return;
-        if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws, static_cast<uint64_t>(nsup) * MN::KMW, N,
+        if (!make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xs_ws, static_cast<uint64_t>(nsup) * MN::KMW, N,
                       static_cast<uint64_t>(nsup) * MN::KMW * 2, 16, BN, CU_TENSOR_MAP_SWIZZLE_32B)) {
             *e = cudaErrorInvalidValue;
             return;
@@ -1390,7 +1475,11 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     a.wq = G ? static_cast<int>(tiles * nsup / G) : 0;
     a.wr = G ? static_cast<int>(tiles * nsup % G) : 0;
     a.Y = p.Y;
-    a.part = G ? reinterpret_cast<float*>(ws + xs_bytes) : nullptr;
+    a.y_dtype = p.y_dtype;
+    a.pair = pair ? 1 : 0;
+    a.ntok = ntok;
+    a.inv_scale = inv_scale;
+    a.part = G ? reinterpret_cast<float*>(xs_ws + xs_bytes) : nullptr;
     a.err = p.err;
     const dim3 grid = G ? dim3(G) : dim3(tiles_m, tiles_n);
     kern<<<grid, kThreads, smem_bytes, s>>>(tmW, tmX, tmB, a);
@@ -1406,7 +1495,7 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* e) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     *e = cudaLaunchKernelEx(&cfg, k_tile_fixup, static_cast<const float*>(a.part), a.Y, M, N, tiles_m, nsup,
-                            tiles * nsup, G);
+                            tiles * nsup, G, p.y_dtype);
     count_launch(1);
     if (*e == cudaSuccess) *e = cudaGetLastError();
 }
@@ -1501,6 +1590,10 @@ void run_noalloc(const Problem& p, cudaStream_t s, int* status) {
     a.wq = 0;
     a.wr = 0;
     a.Y = p.Y;
+    a.y_dtype = p.y_dtype;
+    a.pair = 0;
+    a.ntok = N;
+    a.inv_scale = nullptr;
     a.part = nullptr;   // one tile per CTA: no partial-tile scratch
     a.err = p.err;
     const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);

@@ -107,6 +107,7 @@ struct GemvArgs {
     const void* X;
     int x_dtype;
     float* Y;
+    int y_dtype;              // 0 fp32, 1 f16, 2 bf16
     int ncols;                // plain: N
     // grouped (x_row == nullptr for the plain product)
     const int32_t* x_row;
@@ -1042,7 +1043,7 @@ __device__ __forceinline__ void consume_item(const GemvArgs& a, const Tables& t,
 #pragma unroll
                     for (int w = 0; w < NW; ++w) v += rb[(n * NW + w) * 32 + lane];
                     const int64_t r = a.x_row ? static_cast<int64_t>(t.order[item.col0 + n]) : n;
-                    a.Y[r * a.M + row] = v;
+                    store_y(a.Y, a.y_dtype, r * a.M + row, v);
                 }
             }
         }
@@ -1183,7 +1184,8 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32, MinBlocks<KIND>::V)
             const int nb = T.misc[1], b0 = T.eoff[a.n_experts];
             for (int64_t idx = threadIdx.x; idx < static_cast<int64_t>(nb) * a.M; idx += NW * 32) {
                 const int64_t j = idx / a.M;
-                a.Y[static_cast<int64_t>(T.order[b0 + j]) * a.M + (idx - j * a.M)] = __int_as_float(0x7fc00000);
+                store_y(a.Y, a.y_dtype, static_cast<int64_t>(T.order[b0 + j]) * a.M + (idx - j * a.M),
+                        __int_as_float(0x7fc00000));
             }
             if (threadIdx.x == 0) atomicOr(a.err, DEV_ERR_BAD_INDEX);
         }
@@ -1351,6 +1353,7 @@ cudaError_t launch_nc(const Problem& p, const Plan& pl, cudaStream_t s) {
     a.X = p.X;
     a.x_dtype = p.x_dtype;
     a.Y = p.Y;
+    a.y_dtype = p.y_dtype;
     a.ncols = static_cast<int>(p.N);
     a.x_row = p.x_row;
     a.expert_id = p.expert_id;

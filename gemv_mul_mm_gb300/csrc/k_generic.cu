@@ -102,11 +102,12 @@ __global__ void __launch_bounds__(kWarps * 32) k_generic(Problem p) {
             const int64_t m = m0 + r;
             if (m >= p.M) break;
             if (grouped) {
-                p.Y[static_cast<int64_t>(blockIdx.y) * p.M + m] = bad ? __int_as_float(0x7fc00000) : acc[r][0];
+                store_y(p.Y, p.y_dtype, static_cast<int64_t>(blockIdx.y) * p.M + m,
+                        bad ? __int_as_float(0x7fc00000) : acc[r][0]);
             } else {
 #pragma unroll
                 for (int c = 0; c < NT; ++c)
-                    if (c < ncols) p.Y[xrow[c] * p.M + m] = acc[r][c];
+                    if (c < ncols) store_y(p.Y, p.y_dtype, xrow[c] * p.M + m, acc[r][c]);
             }
         }
         if (bad && warp == 0 && blockIdx.x == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
@@ -124,7 +125,7 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* err) {
             const int64_t nr = imin64(65535, p.N - r0);
             q.x_row = p.x_row + r0;
             q.expert_id = p.expert_id + r0;
-            q.Y = p.Y + r0 * p.M;
+            q.Y = y_at(p.Y, r0 * p.M, p.y_dtype);
             q.N = nr;
             k_generic<KIND, 1><<<dim3(gx, static_cast<unsigned>(nr)), kWarps * 32, 0, s>>>(q);
             count_launch(1);
@@ -138,7 +139,7 @@ void run(const Problem& p, cudaStream_t s, cudaError_t* err) {
         Problem q = p;
         const int64_t nyy = imin64(65535, ny - y0);
         q.X = static_cast<const uint8_t*>(p.X) + y0 * NT * p.K * (p.x_dtype == 1 ? 2 : 4);
-        q.Y = p.Y + y0 * NT * p.M;
+        q.Y = y_at(p.Y, y0 * NT * p.M, p.y_dtype);
         q.N = imin64(p.N - y0 * NT, nyy * NT);
         k_generic<KIND, NT><<<dim3(gx, static_cast<unsigned>(nyy)), kWarps * 32, 0, s>>>(q);
         count_launch(1);

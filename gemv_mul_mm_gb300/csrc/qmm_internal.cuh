@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace qmm {
@@ -46,8 +48,25 @@ struct Problem {
     int n_experts = 0;
     int64_t n_x_rows = 0;
     unsigned flags = 0;      // QMM_FLAG_* of the call
+    int y_dtype = 0;         // output element: 0 fp32, 1 f16, 2 bf16
     unsigned* err = nullptr; // device latch
 };
+
+// Bytes of one output element.
+__host__ __device__ __forceinline__ int y_size(int y_dtype) { return y_dtype == 0 ? 4 : 2; }
+
+// Output element i (of the call's output type) = v, rounded to nearest even
+// for the 16-bit types.
+__device__ __forceinline__ void store_y(float* Y, int y_dtype, int64_t i, float v) {
+    if (y_dtype == 0) Y[i] = v;
+    else if (y_dtype == 1) reinterpret_cast<__half*>(Y)[i] = __float2half_rn(v);
+    else reinterpret_cast<__nv_bfloat16*>(Y)[i] = __float2bfloat16_rn(v);
+}
+
+// Y advanced by `elems` output elements.
+__host__ __device__ __forceinline__ float* y_at(float* Y, int64_t elems, int y_dtype) {
+    return reinterpret_cast<float*>(reinterpret_cast<char*>(Y) + elems * y_size(y_dtype));
+}
 
 // k_selftest.cu : a kernel whose bounded wait runs out (failure-path test)
 cudaError_t launch_wait_never(unsigned* err, long long cycles, cudaStream_t s);

@@ -33,6 +33,8 @@ STATUS_ID = {v: k for k, v in STATUS.items()}
 
 PATH_AUTO, PATH_GENERIC, PATH_GEMV, PATH_TC, PATH_DEQUANT, PATH_GROUPED = 0, 1, 2, 3, 4, 5
 FLAG_WEIGHTS_CONST = 1
+FLAG_Y_F16 = 2
+FLAG_Y_BF16 = 4
 
 
 class QmmError(RuntimeError):
@@ -149,14 +151,27 @@ def qdequant(kind, blocks, rows: int, cols: int, out=None, stream=None):
     return out
 
 
-def qgemm(kind, W, X, M: int, K: int, N: int, Y=None, stream=None, weights_const: bool = False):
-    """Y[n, m] = sum_k W[m, k] X[n, k]; returns Y as an (N, M) fp32 tensor.
+def _yflag(Y) -> int:
+    import torch
+    if Y.dtype == torch.float32:
+        return 0
+    if Y.dtype == torch.float16:
+        return FLAG_Y_F16
+    if Y.dtype == torch.bfloat16:
+        return FLAG_Y_BF16
+    raise TypeError(f"outputs must be float32, float16 or bfloat16, got {Y.dtype}")
+
+
+def qgemm(kind, W, X, M: int, K: int, N: int, Y=None, stream=None, weights_const: bool = False,
+          out_dtype=None):
+    """Y[n, m] = sum_k W[m, k] X[n, k]; returns Y as an (N, M) tensor, fp32
+    unless Y (or out_dtype) is float16 / bfloat16 (rounded once at the store).
     weights_const: W is not written by work still in flight on the stream
     (QMM_FLAG_WEIGHTS_CONST: the GEMV may start streaming it early)."""
     import torch
     if Y is None:
-        Y = torch.empty((N, M), dtype=torch.float32, device=W.device)
-    flags = FLAG_WEIGHTS_CONST if weights_const else 0
+        Y = torch.empty((N, M), dtype=out_dtype or torch.float32, device=W.device)
+    flags = (FLAG_WEIGHTS_CONST if weights_const else 0) | _yflag(Y)
     _check(_lib().qgemm_ex(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(X), _xdt(X),
                            X.numel(), _ptr(Y), Y.numel(), M, K, N, flags, _stream(stream)), "qgemm")
     return Y
@@ -174,15 +189,15 @@ def qgemm_noalloc(kind, W, X, M: int, K: int, N: int, Y=None, stream=None):
     return Y
 
 
-def qgemv(kind, W, x, M: int, K: int, y=None, stream=None, weights_const: bool = False):
+def qgemv(kind, W, x, M: int, K: int, y=None, stream=None, weights_const: bool = False, out_dtype=None):
     """y[m] = sum_k W[m, k] x[k] (qgemm with N = 1)."""
     import torch
     if y is None:
-        y = torch.empty((M,), dtype=torch.float32, device=W.device)
-    if weights_const:
+        y = torch.empty((M,), dtype=out_dtype or torch.float32, device=W.device)
+    flags = (FLAG_WEIGHTS_CONST if weights_const else 0) | _yflag(y)
+    if flags:
         _check(_lib().qgemm_ex(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(x), _xdt(x),
-                               x.numel(), _ptr(y), y.numel(), M, K, 1, FLAG_WEIGHTS_CONST,
-                               _stream(stream)), "qgemv")
+                               x.numel(), _ptr(y), y.numel(), M, K, 1, flags, _stream(stream)), "qgemv")
     else:
         _check(_lib().qgemv(_kind(kind), _ptr(W), W.numel() * W.element_size(), _ptr(x), _xdt(x),
                             x.numel(), _ptr(y), y.numel(), M, K, _stream(stream)), "qgemv")

@@ -147,8 +147,15 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
 /*
  * qgemm -- Y[n * M + m] = sum_k W[m, k] * X[n * K + k] for n < N, m < M
  * (ferrox-cuda mul_mm.rs `BODY_SRC`: src0 = W, src1 = X, dst token-major).
- * Small N runs the weight-streaming GEMV kernels; large N (and f16 activations)
- * the tcgen05 tensor-core GEMM.
+ * Small N runs the weight-streaming GEMV kernels; large N the tcgen05
+ * tensor-core GEMM. fp32 activations reach the tensor cores as two f16 rows
+ * per token: a pre-pass scales each token row by the power of two that puts
+ * its largest magnitude in [2^9, 2^10) and splits it into hi = f16(x) and
+ * lo = f16(x - hi) (together exact to about 2^-22 relative); the epilogue adds
+ * the two products and removes the scale. This doubles the tensor-core work of
+ * the call against f16 activations. With f16 activations, Q4_K, Q5_K and Q2_K
+ * carry the sums of each 32 (Q2_K: 16) consecutive activations in f16: their
+ * magnitudes must stay below 65504.
  *
  *   W, w_bytes   as qgemv
  *   X            device, N * K activations of x_dtype, row-major; x_elems its size
@@ -156,9 +163,11 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
  *
  * Accuracy: |Y - Y_exact| <= 1e-3 * sum_k |W[m,k] * X[n,k]| + 1e-6 per element.
  *
- * Workspace: the tensor-core path keeps two things in a per-device workspace
- * the library owns and grows on demand (cudaMalloc): for Q4_K, Q5_K and Q2_K
- * the per-group activation sums (N * K/16 f16 values at most), and, when the
+ * Workspace: the tensor-core path keeps its scratch in a per-device workspace
+ * the library owns and grows on demand (cudaMalloc): the f16 (hi, lo) rows of
+ * fp32 activations and their scales (4 * N * K + 4 * N bytes), for Q4_K, Q5_K
+ * and Q2_K the per-group activation sums (N * K/16 f16 values at most, twice
+ * that for fp32 activations), and, when the
  * 128 x 128 output tiles do not fill the GPU evenly, the partial tiles of
  * the tiles whose K range several CTAs share (2 * 64 KiB per SM). Those
  * partial sums are added in a fixed order by a second kernel, so results are
@@ -178,7 +187,13 @@ enum {
      * running (programmatic dependent launch); activations are read, and
      * outputs written, only after that kernel has completed, with or without
      * the flag. Other paths ignore it. */
-    QMM_FLAG_WEIGHTS_CONST = 1
+    QMM_FLAG_WEIGHTS_CONST = 1,
+    /* Y holds IEEE binary16 (QMM_FLAG_Y_F16) or bfloat16 (QMM_FLAG_Y_BF16)
+     * values instead of fp32: each output is the fp32 result rounded to
+     * nearest even once, at the store. Y must then be 2-byte aligned and
+     * y_elems counts 16-bit elements. At most one of the two. */
+    QMM_FLAG_Y_F16 = 2,
+    QMM_FLAG_Y_BF16 = 4
 };
 
 /*

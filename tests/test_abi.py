@@ -123,9 +123,18 @@ def test_path_override_is_per_thread(L):
 def test_qgemm_ex_flags(L):
     S = qmm.STATUS_ID
     args = (1, FAKE, 1 << 30, FAKE, 0, 1 << 30, FAKE, 1 << 30, 64, 256)
-    # unknown flag bits are refused before anything else is looked at
-    assert L.qgemm_ex(*args, 1, 2, None) == S["QMM_ERR_BAD_ARGUMENT"]
+    # unknown flag bits, and both 16-bit output types at once, are refused
+    # before anything else is looked at
+    assert L.qgemm_ex(*args, 1, 8, None) == S["QMM_ERR_BAD_ARGUMENT"]
     assert L.qgemm_ex(*args, 1, 0x80000000, None) == S["QMM_ERR_BAD_ARGUMENT"]
+    assert L.qgemm_ex(*args, 1, qmm.FLAG_Y_F16 | qmm.FLAG_Y_BF16, None) == S["QMM_ERR_BAD_ARGUMENT"]
+    # a 16-bit output needs 2-byte alignment, an fp32 one 4-byte
+    for flag, y, want in ((qmm.FLAG_Y_F16, FAKE + 1, "QMM_ERR_MISALIGNED"),
+                          (qmm.FLAG_Y_BF16, FAKE + 1, "QMM_ERR_MISALIGNED"),
+                          (0, FAKE + 2, "QMM_ERR_MISALIGNED"),
+                          (qmm.FLAG_Y_F16, FAKE + 2, "QMM_ERR_COLS_NOT_BLOCK_ALIGNED")):
+        assert L.qgemm_ex(1, FAKE, 1 << 30, FAKE, 0, 1 << 30, y, 1 << 30, 64, 48 if flag else 256, 1, flag,
+                          None) == S[want], (flag, y)
     # the known flag passes validation like qgemm (refused later for the shape)
     assert L.qgemm_ex(1, FAKE, 1 << 30, FAKE, 0, 1 << 30, FAKE, 1 << 30, 64, 48, 1,
                       qmm.FLAG_WEIGHTS_CONST, None) == S["QMM_ERR_COLS_NOT_BLOCK_ALIGNED"]

@@ -542,3 +542,70 @@ def test_grouped_edge_cases(Q, orc, case):
     assert Q.check_device_error() == 0
     y, tol = orc.grouped(kind, w, M * rb, E, x, x_row, eid, M, K)
     assert_within(Y.cpu().numpy(), y, tol, f"grouped {case}")
+
+
+# ---------------------------------------------------------------------------
+# fp32 activations on the tensor-core path, 16-bit outputs
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg,kind", [(synth.KQUANT, "Q4_K"), (synth.KQUANT, "Q6_K"), (synth.KQUANT, "Q2_K"),
+                                      (synth.CODEBOOK, "IQ4_NL"), (synth.CODEBOOK, "MXFP4")])
+def test_prefill_gemm_fp32_activations(Q, orc, cfg, kind):
+    """fp32 activations at the workload shapes run on the tensor cores as
+    (hi, lo) f16 pairs; every output against the oracle."""
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    w = synth.workload_weights(cfg, kind)
+    x = synth.workload_x(cfg, kind).astype(np.float32)
+    x = x + synth.activations(N, K, 123, "f32") * 1e-3      # bits below f16's precision
+    Y = sentinel((N, M))
+    Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
+    assert Q.last_path() == Q.PATH_TC
+    y, tol = oracle_full_product(orc, kind, w, M, K, x)
+    assert_within(Y.cpu().numpy(), y, tol, f"{kind} fp32 X, all {N * M} outputs")
+
+
+@pytest.mark.parametrize("kind", ["Q4_K", "Q5_K", "IQ4_XS", "Q8_0"])
+def test_fp32_activations_of_any_magnitude(Q, orc, kind):
+    """Token rows far outside f16's range (1e30, 1e-30, mixed): the per-row
+    power-of-two scale keeps the (hi, lo) split exact to about 2^-22."""
+    M, K, N = 256, 1024, 40
+    w = synth.quant_weights(kind, M, K, 61)
+    x = synth.activations(N, K, 62, "f32").astype(np.float64)
+    mag = np.array([1e30, 1e-30, 3e4, 7e4, 1e-7, 1.0, 2.0 ** -140, 1e20] * 5)[:N]
+    x = (x * mag[:, None]).astype(np.float32)
+    x[5, 7] = 0.0
+    x[9, :] = 0.0                                            # an all-zero row
+    Y = sentinel((N, M))
+    Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
+    assert Q.last_path() == Q.PATH_TC
+    y, tol = orc.gemm(kind, w, M, K, x, N)
+    assert_within(Y.cpu().numpy(), y, tol, f"{kind} fp32 X wide range")
+
+
+@pytest.mark.parametrize("out", ["f16", "bf16"])
+@pytest.mark.parametrize("kind,N,path", [("Q4_0", 1, "gemv"), ("Q6_K", 3, "gemv"), ("Q4_K", 33, "tc"),
+                                         ("IQ4_NL", 130, "tc_shared"), ("MXFP4", 40, "tc_fp32"),
+                                         ("Q5_0", 5, "generic")])
+def test_sixteen_bit_outputs(Q, orc, out, kind, N, path):
+    """f16 / bf16 outputs are the product rounded once at the store: within
+    the stated bar plus half an ulp of the output type, on every kernel."""
+    import torch
+    M, K = (1000, 4096) if path == "tc_shared" else (300, 2048)
+    xdt = "f32" if path in ("gemv", "generic", "tc_fp32") else "f16"
+    w = synth.quant_weights(kind, M, K, 70 + N)
+    x = synth.activations(N, K, 71 + N, xdt)
+    y, tol = orc.gemm(kind, w, M, K, x, N)
+    tdt = torch.float16 if out == "f16" else torch.bfloat16
+    Y = torch.full((N, M), float("nan"), dtype=tdt, device="cuda")
+    if path == "generic":
+        Q.set_path(Q.PATH_GENERIC)
+    try:
+        Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
+    finally:
+        Q.set_path(0)
+    want_path = {"gemv": Q.PATH_GEMV, "generic": Q.PATH_GENERIC}.get(path, Q.PATH_TC)
+    assert Q.last_path() == want_path
+    got = Y.float().cpu().numpy().astype(np.float64)
+    assert not np.isnan(got).any(), "outputs never written"
+    half_ulp = np.abs(y) * (2.0 ** -11 if out == "f16" else 2.0 ** -8)
+    bad = ~(np.abs(got - y) <= tol + half_ulp)
+    assert not bad.any(), f"{int(bad.sum())} outputs outside the bar"
