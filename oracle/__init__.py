@@ -184,6 +184,12 @@ class Oracle:
         return y, tol
 
 
+    def moe_ffn(self, *args, **kwargs):
+        """The mixture-of-experts layer around the grouped product (oracle/moe.py)."""
+        from . import moe
+        return moe.moe_ffn(self, *args, **kwargs)
+
+
 def load(sabotage: int = 0) -> Oracle:
     if sabotage not in _CACHE:
         _CACHE[sabotage] = Oracle(sabotage)
