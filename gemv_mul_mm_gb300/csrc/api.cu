@@ -148,6 +148,7 @@ const char* qmm_status_str(int status) {
     case QMM_ERR_UNIMPLEMENTED: return "unimplemented";
     case QMM_ERR_BAD_ARGUMENT: return "bad argument";
     case QMM_ERR_OUTPUT_TOO_SMALL: return "output buffer too small";
+    case QMM_ERR_WORKSPACE_TOO_SMALL: return "workspace too small (see qmoe_ffn_workspace_bytes)";
     case QMM_ERR_NOALLOC_LIMIT:
         return "problem needs more scratch than qgemm_noalloc's fixed array holds";
     case QMM_ERR_WORKSPACE_IN_CAPTURE:
@@ -331,6 +332,44 @@ int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X, int x_
     if (x_dtype != QMM_F16 || !gemm_tc_ok(p)) return QMM_ERR_UNIMPLEMENTED;
     const int r = launch_gemm_tc_noalloc(p, static_cast<cudaStream_t>(stream));
     if (r == QMM_OK) t_last_path = 3;
+    return r;
+}
+
+size_t qmoe_ffn_workspace_bytes(int64_t T, int top_k, int64_t d_model, int64_t d_ff) {
+    if (T <= 0 || top_k <= 0 || d_model <= 0 || d_ff <= 0) return 0;
+    return moe_workspace_bytes(T, top_k, d_model, d_ff);
+}
+
+int qmoe_ffn(int kind, const void* W_gu, size_t w_gu_bytes, size_t gu_stride, const void* W_down,
+             size_t w_down_bytes, size_t down_stride, int n_experts, const float* X, size_t x_elems,
+             int64_t T, int64_t d_model, int64_t d_ff, const int32_t* topk_ids, const float* topk_w,
+             int top_k, float* Y, size_t y_elems, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (T < 0 || d_model < 0 || d_ff < 0 || top_k < 0 || n_experts < 0) return QMM_ERR_BAD_ARGUMENT;
+    if (T == 0 || d_model == 0 || d_ff == 0 || top_k == 0) return QMM_ERR_EMPTY_SHAPE;
+    if (!W_gu || !W_down || !X || !topk_ids || !topk_w || !Y || !workspace) return QMM_ERR_NULL_POINTER;
+    if (reinterpret_cast<uintptr_t>(X) % 16 || reinterpret_cast<uintptr_t>(Y) % 4 ||
+        reinterpret_cast<uintptr_t>(topk_ids) % 4 || reinterpret_cast<uintptr_t>(topk_w) % 4 ||
+        reinterpret_cast<uintptr_t>(workspace) % 256)
+        return QMM_ERR_MISALIGNED;
+    const int be = kKinds[kind].block_elems;
+    if (d_model % be || d_ff % be) return QMM_ERR_COLS_NOT_BLOCK_ALIGNED;
+    const size_t rb_gu = qmm_row_bytes(kind, d_model), rb_dn = qmm_row_bytes(kind, d_ff);
+    if (n_experts == 0 || gu_stride / rb_gu < static_cast<size_t>(2 * d_ff) ||
+        down_stride / rb_dn < static_cast<size_t>(d_model))
+        return QMM_ERR_BAD_EXPERT_ID;
+    if (w_gu_bytes < static_cast<size_t>(n_experts - 1) * gu_stride + static_cast<size_t>(2 * d_ff) * rb_gu ||
+        w_down_bytes < static_cast<size_t>(n_experts - 1) * down_stride + static_cast<size_t>(d_model) * rb_dn)
+        return QMM_ERR_WEIGHTS_TOO_SMALL;
+    if (x_elems / static_cast<size_t>(d_model) < static_cast<size_t>(T)) return QMM_ERR_ACTIVATIONS_TOO_SMALL;
+    if (y_elems / static_cast<size_t>(d_model) < static_cast<size_t>(T)) return QMM_ERR_OUTPUT_TOO_SMALL;
+    if (workspace_bytes < moe_workspace_bytes(T, top_k, d_model, d_ff)) return QMM_ERR_WORKSPACE_TOO_SMALL;
+    unsigned* err = nullptr;
+    if (int r = err_ptr(&err)) return r;
+    const int r = launch_moe_ffn(kind, static_cast<const uint8_t*>(W_gu), gu_stride, rb_gu,
+                                 static_cast<const uint8_t*>(W_down), down_stride, rb_dn, n_experts, X, T, d_model,
+                                 d_ff, topk_ids, topk_w, top_k, Y, workspace, err, static_cast<cudaStream_t>(stream));
+    if (r == QMM_OK) t_last_path = 6;
     return r;
 }
 

@@ -108,6 +108,8 @@ struct GemvArgs {
     int x_dtype;
     float* Y;
     int y_dtype;              // 0 fp32, 1 f16, 2 bf16
+    int x_mode;               // 0 plain rows, 1 SwiGLU of gate_up rows (see Problem)
+    int64_t x_stride;         // elements per activation row
     int ncols;                // plain: N
     // grouped (x_row == nullptr for the plain product)
     const int32_t* x_row;
@@ -908,6 +910,8 @@ __device__ void build_tables(const GemvArgs& a, const Tables& t, int64_t rg, int
     __syncwarp();
 }
 
+__device__ __forceinline__ float silu(float v) { return v / (1.f + expf(-v)); }
+
 __device__ __forceinline__ float load_x(const void* X, int xdt, int64_t i) {
     if (xdt == 1) return __half2float(reinterpret_cast<const __half*>(X)[i]);
     return reinterpret_cast<const float*>(X)[i];
@@ -934,8 +938,14 @@ __device__ void stage_x(const GemvArgs& a, const Tables& t, const Item& it, floa
                 const int n = idx / kq, k = 4 * (idx - n * kq);
                 if (n < it.ncol) {
                     const int64_t row = a.x_row ? static_cast<int64_t>(a.x_row[t.order[it.col0 + n]]) : n;
-                    const int64_t off = row * K + k;
-                    if (vec) {
+                    const int64_t off = row * a.x_stride + k;
+                    if (a.x_mode == 1) {
+                        // SwiGLU: gate value k and up value K + k of a gate_up output row
+                        const float* xr = reinterpret_cast<const float*>(a.X) + off;
+                        const float4 g = *reinterpret_cast<const float4*>(xr);
+                        const float4 u = *reinterpret_cast<const float4*>(xr + K);
+                        v[j] = make_float4(silu(g.x) * u.x, silu(g.y) * u.y, silu(g.z) * u.z, silu(g.w) * u.w);
+                    } else if (vec) {
                         v[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.X) + off);
                     } else {
                         v[j].x = load_x(a.X, a.x_dtype, off);
@@ -1256,6 +1266,9 @@ Plan plan(const Problem& p) {
     if (p.K > (1 << 24) || p.K % G::UNIT_E) return pl;
     if (p.row_bytes % 16 || reinterpret_cast<uintptr_t>(p.W) % 16) return pl;
     const bool grouped = p.x_row != nullptr;
+    if (p.x_mode == 1 && (p.x_dtype != 0 || p.K % 4 || p.x_stride % 4 || p.x_stride < 2 * p.K ||
+                          reinterpret_cast<uintptr_t>(p.X) % 16))
+        return pl;
     if (grouped) {
         if (p.expert_stride % 16 || p.n_experts > kMaxGroupedExperts || p.N > kMaxGroupedAssign) return pl;
         // up to four columns per problem: measured on the 64-token MoE
@@ -1354,6 +1367,8 @@ cudaError_t launch_nc(const Problem& p, const Plan& pl, cudaStream_t s) {
     a.x_dtype = p.x_dtype;
     a.Y = p.Y;
     a.y_dtype = p.y_dtype;
+    a.x_mode = p.x_mode;
+    a.x_stride = p.x_stride ? p.x_stride : p.K;
     a.ncols = static_cast<int>(p.N);
     a.x_row = p.x_row;
     a.expert_id = p.expert_id;

@@ -49,6 +49,11 @@ struct Problem {
     int64_t n_x_rows = 0;
     unsigned flags = 0;      // QMM_FLAG_* of the call
     int y_dtype = 0;         // output element: 0 fp32, 1 f16, 2 bf16
+    // activation rows: x_mode 0 reads X[row * K + k]; 1 (SwiGLU, fp32 X with
+    // rows of x_stride >= 2 K values) reads silu(X[row * x_stride + k]) *
+    // X[row * x_stride + K + k]
+    int x_mode = 0;
+    int64_t x_stride = 0;
     unsigned* err = nullptr; // device latch
 };
 
@@ -81,6 +86,13 @@ cudaError_t launch_generic(const Problem& p, cudaStream_t s);
 // the expert-grouped product (p.x_row set)
 bool gemv_stream_ok(const Problem& p);
 cudaError_t launch_gemv_stream(const Problem& p, cudaStream_t s);
+
+// k_moe.cu : the mixture-of-experts layer (qmoe_ffn)
+size_t moe_workspace_bytes(int64_t T, int top_k, int64_t d_model, int64_t d_ff);
+int launch_moe_ffn(int kind, const uint8_t* W_gu, size_t gu_stride, size_t gu_row_bytes, const uint8_t* W_down,
+                   size_t down_stride, size_t down_row_bytes, int n_experts, const float* X, int64_t T,
+                   int64_t d_model, int64_t d_ff, const int32_t* ids, const float* w, int top_k, float* Y,
+                   void* workspace, unsigned* err, cudaStream_t s);
 
 // k_gemm_tc.cu : tcgen05 tensor-core GEMM
 bool gemm_tc_ok(const Problem& p);

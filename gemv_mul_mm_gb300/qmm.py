@@ -27,11 +27,11 @@ STATUS = {
     6: "QMM_ERR_ACTIVATIONS_TOO_SMALL", 7: "QMM_ERR_NULL_POINTER", 8: "QMM_ERR_MISALIGNED",
     9: "QMM_ERR_BAD_EXPERT_ID", 10: "QMM_ERR_CUDA", 11: "QMM_ERR_DEVICE_TIMEOUT",
     12: "QMM_ERR_UNIMPLEMENTED", 13: "QMM_ERR_BAD_ARGUMENT", 14: "QMM_ERR_OUTPUT_TOO_SMALL",
-    15: "QMM_ERR_WORKSPACE_IN_CAPTURE", 16: "QMM_ERR_NOALLOC_LIMIT",
+    15: "QMM_ERR_WORKSPACE_IN_CAPTURE", 16: "QMM_ERR_NOALLOC_LIMIT", 17: "QMM_ERR_WORKSPACE_TOO_SMALL",
 }
 STATUS_ID = {v: k for k, v in STATUS.items()}
 
-PATH_AUTO, PATH_GENERIC, PATH_GEMV, PATH_TC, PATH_DEQUANT, PATH_GROUPED = 0, 1, 2, 3, 4, 5
+PATH_AUTO, PATH_GENERIC, PATH_GEMV, PATH_TC, PATH_DEQUANT, PATH_GROUPED, PATH_MOE = 0, 1, 2, 3, 4, 5, 6
 FLAG_WEIGHTS_CONST = 1
 FLAG_Y_F16 = 2
 FLAG_Y_BF16 = 4
@@ -68,6 +68,10 @@ def _lib():
         L.qgemm_noalloc.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _I64, _P]
         L.qgemm_grouped.argtypes = [_I, _P, _SZ, _SZ, _I, _P, _I, _SZ, _I64, _P, _P, _I64,
                                     _P, _SZ, _I64, _I64, _P]
+        L.qmoe_ffn.argtypes = [_I, _P, _SZ, _SZ, _P, _SZ, _SZ, _I, _P, _SZ, _I64, _I64, _I64, _P, _P, _I,
+                               _P, _SZ, _P, _SZ, _P]
+        L.qmoe_ffn_workspace_bytes.argtypes = [_I64, _I, _I64, _I64]
+        L.qmoe_ffn_workspace_bytes.restype = _SZ
         L.qmm_check_device_error.argtypes = [_P]
         L.qmm_selftest_wait_timeout.argtypes = [_I64, _P]
         L.qmm_set_path.argtypes = [_I]
@@ -216,6 +220,30 @@ def qgemm_grouped(kind, W, expert_stride: int, n_experts: int, X, x_row, expert_
                                 n_experts, _ptr(X), _xdt(X), X.numel(), n_x_rows, _ptr(x_row),
                                 _ptr(expert_id), n_assign, _ptr(Y), Y.numel(), M, K,
                                 _stream(stream)), "qgemm_grouped")
+    return Y
+
+
+def qmoe_ffn_workspace_bytes(T: int, top_k: int, d_model: int, d_ff: int) -> int:
+    return _lib().qmoe_ffn_workspace_bytes(T, top_k, d_model, d_ff)
+
+
+def qmoe_ffn(kind, W_gu, gu_stride: int, W_down, down_stride: int, n_experts: int, X, topk_ids, topk_w,
+             d_model: int, d_ff: int, Y=None, workspace=None, stream=None):
+    """One MoE feed-forward layer: Y[t] = sum_j w[t, j] W_down_e (silu(g) * u),
+    (g, u) = W_gu_e x_t, e = topk_ids[t, j]; returns Y as (T, d_model) fp32.
+    The scratch comes from `workspace` (a CUDA uint8 tensor of at least
+    qmoe_ffn_workspace_bytes(...) bytes), allocated here with torch if None."""
+    import torch
+    T, top_k = topk_ids.shape
+    if Y is None:
+        Y = torch.empty((T, d_model), dtype=torch.float32, device=W_gu.device)
+    need = qmoe_ffn_workspace_bytes(T, top_k, d_model, d_ff)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=W_gu.device)
+    _check(_lib().qmoe_ffn(_kind(kind), _ptr(W_gu), W_gu.numel() * W_gu.element_size(), gu_stride,
+                           _ptr(W_down), W_down.numel() * W_down.element_size(), down_stride, n_experts,
+                           _ptr(X), X.numel(), T, d_model, d_ff, _ptr(topk_ids), _ptr(topk_w), top_k,
+                           _ptr(Y), Y.numel(), _ptr(workspace), workspace.numel(), _stream(stream)), "qmoe_ffn")
     return Y
 
 

@@ -246,3 +246,21 @@ def moe_problem(T: int, which: str = "gate_up", seed: int = None):
         x_row = np.arange(T * top, dtype=np.int32)
     return dict(kind=kind, w=w, stride=stride, n_experts=E, x=x, x_row=x_row,
                 expert_id=expert_id, M=M, K=K)
+
+
+def moe_layer_problem(T: int, seed: int = None):
+    """One MoE layer of the config-4 shape: both projections' weights for all
+    experts, fp32 tokens, per-token top-k expert ids (distinct, seeded) and
+    routing weights (uniform draws normalised to sum to one per token)."""
+    cfg = MOE
+    kind, E, k = cfg["kind"], cfg["n_experts"], cfg["top_k"]
+    dm, dff = cfg["d_model"], cfg["d_ff"]
+    seed = config_seed(4, kind) + 5000 + T if seed is None else seed
+    w_gu = quant_weights(kind, E * 2 * dff, dm, config_seed(4, kind))
+    w_dn = quant_weights(kind, E * dm, dff, config_seed(4, kind) + 7)
+    ids = routing(T, E, k, seed)
+    wt = Stream(substream(seed, 8)).uniform(T * k, 0.05, 1.0).reshape(T, k)
+    wt = (wt / wt.sum(axis=1, keepdims=True)).astype(np.float32)
+    x = activations(T, dm, seed + 3, "f32")
+    return dict(kind=kind, w_gu=w_gu, gu_stride=2 * dff * row_bytes(kind, dm), w_down=w_dn,
+                down_stride=dm * row_bytes(kind, dff), n_experts=E, x=x, ids=ids, w=wt, d_model=dm, d_ff=dff)

@@ -93,7 +93,8 @@ typedef enum {
     QMM_ERR_BAD_ARGUMENT = 13,           /* negative size or other bad scalar */
     QMM_ERR_OUTPUT_TOO_SMALL = 14,       /* y_elems < outputs to write */
     QMM_ERR_WORKSPACE_IN_CAPTURE = 15,   /* workspace would grow during stream capture */
-    QMM_ERR_NOALLOC_LIMIT = 16           /* qgemm_noalloc: scratch needed exceeds its fixed array */
+    QMM_ERR_NOALLOC_LIMIT = 16,          /* qgemm_noalloc: scratch needed exceeds its fixed array */
+    QMM_ERR_WORKSPACE_TOO_SMALL = 17     /* caller-provided workspace smaller than required */
 } qmm_status;
 
 /* Geometry of `kind`: bytes and elements of one block. Returns QMM_OK or
@@ -264,6 +265,51 @@ QMM_API int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert
                   float* Y, size_t y_elems, int64_t M, int64_t K, void* stream);
 
 /*
+ * qmoe_ffn -- one mixture-of-experts feed-forward layer over block-quantized
+ * experts (the decoder layer whose per-token weight traffic the inferencelayer
+ * 0.2.8 src/cublas_prefill.rs page quotes for Qwen3-30B-A3B). For token t and
+ * routing slot j < top_k, with e = topk_ids[t * top_k + j] and weight
+ * topk_w[t * top_k + j]:
+ *
+ *   g, u = rows [0, d_ff) and [d_ff, 2 d_ff) of W_gu_e times x_t
+ *   h    = silu(g) * u,   silu(v) = v / (1 + e^-v)          (SwiGLU)
+ *   o    = W_down_e h
+ *   Y[t] = sum_j topk_w[t * top_k + j] * o                 (in slot order)
+ *
+ * The projections run on the expert-grouped streaming GEMV (each touched
+ * expert's rows stream once per block of up to four of its assignments); the
+ * down projection computes silu(g) * u while it stages its activations. The
+ * routing weights are applied as given (normalise them first if the model
+ * does). Accuracy: within what qgemm's per-product bar implies through SwiGLU
+ * and the down projection.
+ *
+ *   W_gu, w_gu_bytes     device, n_experts experts every gu_stride bytes, each
+ *                        2 d_ff rows of d_model elements (gate rows first)
+ *   W_down, w_down_bytes device, experts every down_stride bytes, each d_model
+ *                        rows of d_ff elements
+ *   X                    device fp32 [T][d_model], 16-byte aligned
+ *   topk_ids, topk_w     device int32 / fp32 [T][top_k]; an expert id out of
+ *                        range gives NaN in its token's row of Y and latches
+ *                        QMM_ERR_BAD_EXPERT_ID for qmm_check_device_error()
+ *   Y                    device fp32 [T][d_model]
+ *   workspace            device scratch owned by the caller, 256-byte aligned,
+ *                        at least qmoe_ffn_workspace_bytes(T, top_k, d_model,
+ *                        d_ff) bytes; the library allocates nothing. Calls that
+ *                        overlap on the GPU must not share a workspace.
+ *
+ * Both projections must take the streaming kernel: 16-byte aligned weights,
+ * strides and rows that are multiples of 16 bytes, n_experts <= 1024 and
+ * T * top_k <= 4096 (QMM_ERR_UNIMPLEMENTED otherwise).
+ */
+QMM_API int qmoe_ffn(int kind, const void* W_gu, size_t w_gu_bytes, size_t gu_stride, const void* W_down,
+                     size_t w_down_bytes, size_t down_stride, int n_experts, const float* X, size_t x_elems,
+                     int64_t T, int64_t d_model, int64_t d_ff, const int32_t* topk_ids, const float* topk_w,
+                     int top_k, float* Y, size_t y_elems, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Scratch bytes qmoe_ffn needs for these sizes (0 for a non-positive size). */
+QMM_API size_t qmoe_ffn_workspace_bytes(int64_t T, int top_k, int64_t d_model, int64_t d_ff);
+
+/*
  * qmm_check_device_error -- synchronize `stream`, then read and clear the
  * device-side error latch of the current device. Returns QMM_OK,
  * QMM_ERR_DEVICE_TIMEOUT (a bounded wait in a kernel ran out; that kernel's
@@ -292,7 +338,7 @@ QMM_API int qmm_set_path(int path);
 
 /* Which kernel family the most recent successful call on this host thread
  * launched: 1 generic, 2 streaming GEMV, 3 tensor-core GEMM, 4 dequant,
- * 5 grouped GEMV; 0 before any call. */
+ * 5 grouped GEMV, 6 MoE layer; 0 before any call. */
 QMM_API int qmm_last_path(void);
 
 /* Number of kernels this library has launched since load (all threads). */

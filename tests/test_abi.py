@@ -39,7 +39,7 @@ def test_kind_table(L):
 
 
 def test_status_strings(L):
-    for code in range(17):
+    for code in range(18):
         assert L.qmm_status_str(code)
     assert L.qmm_status_str(999) == b"unknown status"
 
@@ -144,3 +144,32 @@ def test_selftest_refuses_bad_cycle_counts(L):
     import ctypes
     for bad in (0, -5, (1 << 32) + 1):
         assert L.qmm_selftest_wait_timeout(ctypes.c_int64(bad), None) == 13   # QMM_ERR_BAD_ARGUMENT
+
+
+def test_moe_layer_refusals(L):
+    S = qmm.STATUS_ID
+    rb_gu, rb_dn = 8 * 18, 24 * 18      # Q4_0, d_model 256, d_ff 768
+
+    def m(**kw):
+        a = dict(kind=1, gu=FAKE, gub=1 << 30, gus=2 * 768 * rb_gu, dn=FAKE, dnb=1 << 30, dns=256 * rb_dn,
+                 ne=4, x=FAKE, xe=1 << 20, T=2, dm=256, dff=768, ids=FAKE, w=FAKE, k=2, y=FAKE, ye=1 << 20,
+                 ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return L.qmoe_ffn(a["kind"], a["gu"], a["gub"], a["gus"], a["dn"], a["dnb"], a["dns"], a["ne"], a["x"],
+                          a["xe"], a["T"], a["dm"], a["dff"], a["ids"], a["w"], a["k"], a["y"], a["ye"], a["ws"],
+                          a["wsb"], None)
+    assert m(kind=11) == S["QMM_ERR_BAD_KIND"]
+    assert m(T=0) == S["QMM_ERR_EMPTY_SHAPE"]
+    assert m(k=-1) == S["QMM_ERR_BAD_ARGUMENT"]
+    assert m(ids=0) == S["QMM_ERR_NULL_POINTER"]
+    assert m(ws=FAKE + 16) == S["QMM_ERR_MISALIGNED"]
+    assert m(x=FAKE + 4) == S["QMM_ERR_MISALIGNED"]
+    assert m(dff=760) == S["QMM_ERR_COLS_NOT_BLOCK_ALIGNED"]
+    assert m(gus=2 * 768 * rb_gu - 1) == S["QMM_ERR_BAD_EXPERT_ID"]
+    assert m(dnb=3 * 256 * rb_dn + 256 * rb_dn - 1) == S["QMM_ERR_WEIGHTS_TOO_SMALL"]
+    assert m(xe=2 * 256 - 1) == S["QMM_ERR_ACTIVATIONS_TOO_SMALL"]
+    assert m(ye=2 * 256 - 1) == S["QMM_ERR_OUTPUT_TOO_SMALL"]
+    need = qmm.qmoe_ffn_workspace_bytes(2, 2, 256, 768)
+    assert need > 4 * 2 * (2 * 768 + 256)
+    assert m(wsb=need - 1) == S["QMM_ERR_WORKSPACE_TOO_SMALL"]
+    assert qmm.qmoe_ffn_workspace_bytes(0, 2, 256, 768) == 0
