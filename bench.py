@@ -378,6 +378,37 @@ def secondary_table(qmm, synth, l2_bytes, stream, pk):
             gemv[kind] = {"error": f"{type(e).__name__}: {e}"[:200]}
     out["gemv"] = gemv
 
+    # load-time repacked layout (Q8_0, Q4_0): the decode shape, and a shape
+    # with few rows (M 2048, K 14336: 64 row groups on the SMs) where the
+    # reduction over K is split; the native streaming GEMV beside it
+    rep = {}
+    for kind in ("Q8_0", "Q4_0"):
+        for (M2, K2) in ((c["M"], c["K"]), (2048, 14336)):
+            try:
+                wh = synth.quant_weights(kind, M2, K2, synth.config_seed(1, kind) + M2)
+                xh = synth.activations(1, K2, 17 + M2, "f32")
+                ws, copies = rot(wh, wh.size)
+                rs = [qmm.qrepack(kind, w_, M2, K2) for w_ in ws]
+                x = torch.from_numpy(xh).cuda()
+                y = torch.empty(M2, device="cuda")
+                row = {"M": M2, "K": K2}
+                for name, fn in (("native", lambda i: qmm.qgemv(kind, ws[i], x, M2, K2, y=y, stream=sh,
+                                                                 weights_const=True)),
+                                 ("repacked", lambda i: qmm.qgemm_repacked(kind, rs[i], x, M2, K2, 1, Y=y, stream=sh,
+                                                                           weights_const=True))):
+                    bm = bench_graph(fn, copies, stream, reps=max(copies, 20))
+                    alg = wh.size + 4 * K2 + 4 * M2
+                    row[name] = dict(**_us(bm), weight_gbs=round(wh.size / (bm[0] * 1e-3) / 1e9, 1),
+                                     frac_of_hbm=round(alg / (bm[0] * 1e-3) / 1e9 / pk["hbm_gbs"], 4))
+                torch.cuda.synchronize()
+                jobs.append(dict(what="gemm_full", tag=f"repacked_{kind}_M{M2}", kind=kind, w=wh, x=xh, M=M2, K=K2,
+                                 N=1, got=y.cpu().numpy().reshape(1, M2)))
+                rep[f"{kind}_M{M2}_K{K2}"] = row
+                del ws, rs
+            except Exception as e:
+                rep[f"{kind}_M{M2}_K{K2}"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    out["repacked_gemv"] = rep
+
     deq = {}
 
     def dequant_row(kind, ws, copies, M, K, wh):

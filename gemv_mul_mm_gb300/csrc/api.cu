@@ -170,7 +170,7 @@ int qmm_last_path(void) { return t_last_path; }
 uint64_t qmm_launch_count(void) { return g_launches.load(); }
 
 int qmm_shutdown(void) {
-    const bool ok = qmm::release_gemm_workspaces();
+    const bool ok = qmm::release_gemm_workspaces() & qmm::release_split_workspaces();
     // device addresses of the library's __device__ arrays are looked up again
     // on the next call (a new context may place them elsewhere)
     qmm::forget_symbol_addresses();
@@ -332,6 +332,66 @@ int qgemm_noalloc(int kind, const void* W, size_t w_bytes, const void* X, int x_
     if (x_dtype != QMM_F16 || !gemm_tc_ok(p)) return QMM_ERR_UNIMPLEMENTED;
     const int r = launch_gemm_tc_noalloc(p, static_cast<cudaStream_t>(stream));
     if (r == QMM_OK) t_last_path = 3;
+    return r;
+}
+
+size_t qrepack_bytes(int kind, int64_t rows, int64_t cols) {
+    if (!kind_ok(kind)) return 0;
+    return repack_bytes(kind, rows, cols);
+}
+
+int qrepack(int kind, const void* W, size_t w_bytes, int64_t rows, int64_t cols, void* out, size_t out_bytes,
+            void* stream) {
+    if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (kind != QMM_Q8_0 && kind != QMM_Q4_0) return QMM_ERR_UNIMPLEMENTED;
+    if (rows < 0 || cols < 0) return QMM_ERR_BAD_ARGUMENT;
+    if (rows == 0 || cols == 0) return QMM_ERR_EMPTY_SHAPE;
+    if (!W || !out) return QMM_ERR_NULL_POINTER;
+    if (cols % 256) return QMM_ERR_COLS_NOT_BLOCK_ALIGNED;
+    const size_t need = repack_bytes(kind, rows, cols);
+    if (w_bytes < need) return QMM_ERR_WEIGHTS_TOO_SMALL;
+    if (out_bytes < need) return QMM_ERR_OUTPUT_TOO_SMALL;
+    return finish(launch_repack(kind, static_cast<const uint8_t*>(W), rows, cols, static_cast<uint8_t*>(out),
+                                static_cast<cudaStream_t>(stream)), 4);
+}
+
+int qgemm_repacked(int kind, const void* R, size_t r_bytes, const void* X, int x_dtype, size_t x_elems, float* Y,
+                   size_t y_elems, int64_t M, int64_t K, int64_t N, int split, uint32_t flags, void* stream) {
+    if (!kind_ok(kind)) return QMM_ERR_BAD_KIND;
+    if (kind != QMM_Q8_0 && kind != QMM_Q4_0) return QMM_ERR_UNIMPLEMENTED;
+    constexpr uint32_t kKnown = QMM_FLAG_WEIGHTS_CONST | QMM_FLAG_Y_F16 | QMM_FLAG_Y_BF16;
+    if ((flags & ~kKnown) || ((flags & QMM_FLAG_Y_F16) && (flags & QMM_FLAG_Y_BF16))) return QMM_ERR_BAD_ARGUMENT;
+    const int y_dtype = (flags & QMM_FLAG_Y_F16) ? 1 : (flags & QMM_FLAG_Y_BF16) ? 2 : 0;
+    if (M < 0 || K < 0 || N < 0 || split < 0) return QMM_ERR_BAD_ARGUMENT;
+    if (M == 0 || K == 0 || N == 0) return QMM_ERR_EMPTY_SHAPE;
+    if (!R || !X || !Y) return QMM_ERR_NULL_POINTER;
+    if (int r = check_x(X, x_dtype)) return r;
+    if (reinterpret_cast<uintptr_t>(Y) % y_size(y_dtype) || reinterpret_cast<uintptr_t>(R) % 16)
+        return QMM_ERR_MISALIGNED;
+    if (K % 256) return QMM_ERR_COLS_NOT_BLOCK_ALIGNED;
+    if (N > 8) return QMM_ERR_UNIMPLEMENTED;
+    if (split > 0 && (K / 256) % split) return QMM_ERR_BAD_ARGUMENT;
+    const size_t rb = qmm_row_bytes(kind, K);
+    if (r_bytes / rb < static_cast<size_t>(M)) return QMM_ERR_WEIGHTS_TOO_SMALL;
+    if (x_elems / static_cast<size_t>(K) < static_cast<size_t>(N)) return QMM_ERR_ACTIVATIONS_TOO_SMALL;
+    if (y_elems / static_cast<size_t>(M) < static_cast<size_t>(N)) return QMM_ERR_OUTPUT_TOO_SMALL;
+    unsigned* err = nullptr;
+    if (int r = err_ptr(&err)) return r;
+    Problem p;
+    p.kind = kind == QMM_Q8_0 ? kRepackedQ8_0 : kRepackedQ4_0;
+    p.W = static_cast<const uint8_t*>(R);
+    p.row_bytes = rb;
+    p.M = M;
+    p.K = K;
+    p.N = N;
+    p.X = X;
+    p.x_dtype = x_dtype;
+    p.Y = Y;
+    p.y_dtype = y_dtype;
+    p.flags = flags;
+    p.err = err;
+    const int r = launch_gemv_split(p, split, static_cast<cudaStream_t>(stream));
+    if (r == QMM_OK) t_last_path = 7;
     return r;
 }
 

@@ -24,7 +24,11 @@ namespace qmm {
 
 enum Kind : int {
     Q8_0 = 0, Q4_0 = 1, Q5_0 = 2, Q4_K = 3, Q5_K = 4, Q6_K = 5,
-    Q2_K = 6, Q3_K = 7, IQ4_NL = 8, IQ4_XS = 9, MXFP4 = 10, NKINDS = 11
+    Q2_K = 6, Q3_K = 7, IQ4_NL = 8, IQ4_XS = 9, MXFP4 = 10, NKINDS = 11,
+    // Library-internal layouts made by qrepack (not block formats of the ABI):
+    // Q8_0 / Q4_0 rows as units of eight blocks, the eight code fields back to
+    // back (32 / 16 bytes each) and then the eight f16 scales (16 bytes).
+    Q8_0R = 11, Q4_0R = 12
 };
 
 template <int KIND> struct Geo;
@@ -39,6 +43,8 @@ template <> struct Geo<Q3_K>   { static constexpr int BB = 110, BE = 256; };
 template <> struct Geo<IQ4_NL> { static constexpr int BB = 18,  BE = 32;  };
 template <> struct Geo<IQ4_XS> { static constexpr int BB = 136, BE = 256; };
 template <> struct Geo<MXFP4>  { static constexpr int BB = 17,  BE = 32;  };
+template <> struct Geo<Q8_0R>  { static constexpr int BB = 34,  BE = 32;  };
+template <> struct Geo<Q4_0R>  { static constexpr int BB = 18,  BE = 32;  };
 
 // 16-entry codebooks. IQ4_NL/IQ4_XS values and the E2M1 values (code 8 is
 // negative zero) as the codebook.rs page lists them.
@@ -296,6 +302,15 @@ __device__ __forceinline__ float2 scale256(const uint8_t* b) {
     else if constexpr (KIND == Q3_K) return make_float2(h2f(ld16(b, 108)), 0.f);
     else return make_float2(h2f(ld16(b, 0)), 0.f);  // IQ4_XS
 }
+
+// Runtime kind -> template dispatch helper for the streaming GEMV, which also
+// reads the repacked layouts.
+#define QMM_DISPATCH_GEMV_KIND(kind, FN, ...)                     \
+    switch (kind) {                                               \
+    case ::qmm::Q8_0R: FN<::qmm::Q8_0R>(__VA_ARGS__); break;      \
+    case ::qmm::Q4_0R: FN<::qmm::Q4_0R>(__VA_ARGS__); break;      \
+    default: QMM_DISPATCH_KIND(kind, FN, __VA_ARGS__);            \
+    }
 
 // Runtime kind -> template dispatch helper.
 #define QMM_DISPATCH_KIND(kind, FN, ...)                          \

@@ -92,6 +92,8 @@ template <> struct SG<Q6_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; 
 template <> struct SG<Q2_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
 template <> struct SG<Q3_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
 template <> struct SG<IQ4_XS> { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
+template <> struct SG<Q8_0R>  { static constexpr int UB = 8,  NW = 8,  NWU = 4; };
+template <> struct SG<Q4_0R>  { static constexpr int UB = 8,  NW = 16, NWU = 8; };
 
 template <int KIND> struct SGeo {
     static constexpr int NW = SG<KIND>::NW;
@@ -720,6 +722,88 @@ __device__ __forceinline__ void unit_iq4xs(const uint8_t* u, const float* xs, in
     }
 }
 
+// Repacked Q4_0 (qrepack): a unit is the 16 code bytes of eight blocks, then
+// their eight f16 scales; every code word is aligned, so each block decodes
+// like the odd blocks of the native layout (same nibble-in-mantissa trick,
+// activations staged in that order). Rolled over block pairs.
+template <int NC>
+__device__ __forceinline__ void unit_q4_0r(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+    const uint32_t mask[5] = {0xFu, 0xF0u, 0xF00u, 0xF000u, 0xF0000u};
+    const uint32_t kMagic = 0x43000000u;   // 128.0f
+    const float2 nb0 = make_float2(-(128.f + 8.f * 0x1p-16f), -(128.f + 8.f * 0x1p-12f));
+    const float2 nb1 = make_float2(-(128.f + 8.f * 0x1p-8f), -(128.f + 8.f * 0x1p-4f));
+    const float2 nb2 = make_float2(-136.f, -(128.f + 8.f * 0x1p-8f));
+    const float2 nb3 = make_float2(-(128.f + 8.f * 0x1p-4f), -136.f);
+    const uint4 sv = *reinterpret_cast<const uint4*>(u + 128);
+#pragma unroll 1
+    for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t sp = pr == 0 ? sv.x : pr == 1 ? sv.y : pr == 2 ? sv.z : sv.w;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(u + 32 * pr);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(u + 32 * pr + 16);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t words[4] = {h ? c1.x : c0.x, h ? c1.y : c0.y, h ? c1.z : c0.z, h ? c1.w : c0.w};
+            const float d = h2f(h ? (sp >> 16) : sp);
+            const int kb = k0 + 32 * (2 * pr + h);
+            float2 S[NC][2];
+#pragma unroll
+            for (int n = 0; n < NC; ++n) S[n][0] = S[n][1] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t v = words[j], sh = v >> 12;
+                const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[0], kMagic)),
+                                                          __uint_as_float(and_or(v, mask[1], kMagic))), nb0);
+                const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[2], kMagic)),
+                                                          __uint_as_float(and_or(v, mask[3], kMagic))), nb1);
+                const float2 f45 = __fadd2_rn(make_float2(__uint_as_float(and_or(v, mask[4], kMagic)),
+                                                          __uint_as_float(and_or(sh, mask[2], kMagic))), nb2);
+                const float2 f67 = __fadd2_rn(make_float2(__uint_as_float(and_or(sh, mask[3], kMagic)),
+                                                          __uint_as_float(and_or(sh, mask[4], kMagic))), nb3);
+#pragma unroll
+                for (int n = 0; n < NC; ++n) {
+                    const float4 xl = *reinterpret_cast<const float4*>(xs + n * K + kb + 8 * j);
+                    const float4 xh = *reinterpret_cast<const float4*>(xs + n * K + kb + 8 * j + 4);
+                    S[n][0] = __ffma2_rn(f01, make_float2(xl.x, xl.y), S[n][0]);
+                    S[n][1] = __ffma2_rn(f23, make_float2(xl.z, xl.w), S[n][1]);
+                    S[n][0] = __ffma2_rn(f45, make_float2(xh.x, xh.y), S[n][0]);
+                    S[n][1] = __ffma2_rn(f67, make_float2(xh.z, xh.w), S[n][1]);
+                }
+            }
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                const float2 t2 = __fadd2_rn(S[n][0], S[n][1]);
+                acc[n] = fmaf(d, t2.x + t2.y, acc[n]);
+            }
+        }
+    }
+}
+
+// Repacked Q8_0: the 32 code bytes of eight blocks, then their eight f16
+// scales. Rolled over block pairs; codes in natural order.
+template <int NC>
+__device__ __forceinline__ void unit_q8_0r(const uint8_t* u, const float* xs, int K, int k0, float (&acc)[NC]) {
+    const float2 nb = nbias(128.f);
+    const uint4 sv = *reinterpret_cast<const uint4*>(u + 256);
+#pragma unroll 1
+    for (int pr = 0; pr < 4; ++pr) {
+        const uint32_t sp = pr == 0 ? sv.x : pr == 1 ? sv.y : pr == 2 ? sv.z : sv.w;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 c0 = *reinterpret_cast<const uint4*>(u + 64 * pr + 32 * h);
+            const uint4 c1 = *reinterpret_cast<const uint4*>(u + 64 * pr + 32 * h + 16);
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const int kb = k0 + 32 * (2 * pr + h);
+            float2 S[NC];
+            zero2(S);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dot4<NC>(w[i] ^ 0x80808080u, nb, xs + kb + 4 * i, K, S);   // int8 + 128
+            const float d = h2f(h ? (sp >> 16) : sp);
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[n] = fmaf(d, S[n].x + S[n].y, acc[n]);
+        }
+    }
+}
+
 template <int KIND, int NC>
 __device__ __forceinline__ void unit(const uint8_t* u, const float* xs, const float* xsum, int K, int k0,
                                      float (&acc)[NC]) {
@@ -730,6 +814,10 @@ __device__ __forceinline__ void unit(const uint8_t* u, const float* xs, const fl
     } else if constexpr (KIND == Q8_0) {
         static_assert(SG<KIND>::UB == 8, "the Q8_0 decoder takes eight blocks");
         unit_q8_0<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == Q4_0R) {
+        unit_q4_0r<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == Q8_0R) {
+        unit_q8_0r<NC>(u, xs, K, k0, acc);
     } else if constexpr (KIND == Q5_0) {
         static_assert(SG<KIND>::UB == 8, "the Q5_0 decoder takes eight blocks");
         unit_q5_0<NC>(u, xs, K, k0, acc);
@@ -921,8 +1009,8 @@ __device__ __forceinline__ float load_x(const void* X, int xdt, int64_t i) {
 // the format's layout. Consumers only. Each thread issues a batch of eight
 // 16-byte loads before it stores any of them, so the staging costs one L2
 // round trip per batch instead of one per load.
-template <int KIND, int NCMAX>
-__device__ void stage_x(const GemvArgs& a, const Tables& t, const Item& it, float* xs, int tid, int nthr) {
+template <int KIND, int NCMAX, bool SWIGLU>
+__device__ void stage_x_rows(const GemvArgs& a, const Tables& t, const Item& it, float* xs, int tid, int nthr) {
     constexpr int B = 8;
     const int K = a.K;
     const int kq = K / 4;
@@ -938,9 +1026,9 @@ __device__ void stage_x(const GemvArgs& a, const Tables& t, const Item& it, floa
                 const int n = idx / kq, k = 4 * (idx - n * kq);
                 if (n < it.ncol) {
                     const int64_t row = a.x_row ? static_cast<int64_t>(a.x_row[t.order[it.col0 + n]]) : n;
-                    const int64_t off = row * a.x_stride + k;
-                    if (a.x_mode == 1) {
-                        // SwiGLU: gate value k and up value K + k of a gate_up output row
+                    const int64_t off = row * (SWIGLU ? a.x_stride : static_cast<int64_t>(K)) + k;
+                    if constexpr (SWIGLU) {
+                        // gate value k and up value K + k of a gate_up output row
                         const float* xr = reinterpret_cast<const float*>(a.X) + off;
                         const float4 g = *reinterpret_cast<const float4*>(xr);
                         const float4 u = *reinterpret_cast<const float4*>(xr + K);
@@ -961,12 +1049,13 @@ __device__ void stage_x(const GemvArgs& a, const Tables& t, const Item& it, floa
             const int idx = base + j * nthr;
             if (idx >= total) continue;   // (no break: the loop must unroll, v[] stays in registers)
             const int n = idx / kq, k = 4 * (idx - n * kq);
-            if constexpr (KIND == Q4_0) {
+            if constexpr (KIND == Q4_0 || KIND == Q4_0R) {
                 const float vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int kk = k + c, b = kk >> 5, e = kk & 31;
-                    const int slot = q4_slot(e, (b & 1) == 0);
+                    // native even blocks start 2 bytes off a word; repacked codes are all aligned
+                    const int slot = q4_slot(e, KIND == Q4_0 && (b & 1) == 0);
                     // times 2^-p, an exact power-of-two product
                     xs[n * K + 32 * b + slot] = vv[c] * __int_as_float((127 - q4_pow(slot & 7)) << 23);
                 }
@@ -986,6 +1075,7 @@ __device__ void stage_x(const GemvArgs& a, const Tables& t, const Item& it, floa
         }
     }
 }
+
 
 // Per-16 activation sums (sequential fp32 adds over the staged values, in
 // natural order) for the formats with a minimum term: xsum[n * K / 16 + g].
@@ -1065,9 +1155,14 @@ __device__ __forceinline__ void consume_item(const GemvArgs& a, const Tables& t,
 // Q4_0 (17 warps) gets the registers of one CTA per SM: its decoder spills at
 // the 60 registers two such CTAs would allow. The other formats keep room for
 // a second CTA (the next kernel's, under programmatic dependent launch).
-template <int KIND> struct MinBlocks { static constexpr int V = (KIND == Q4_0) ? 1 : 2; };
+template <int KIND> struct MinBlocks { static constexpr int V = (KIND == Q4_0 || KIND == Q4_0R) ? 1 : 2; };
 
-template <int KIND, int NCMAX>
+// SWI: the activations are SwiGLU of gate_up rows (the MoE down projection).
+// A template parameter, not a runtime mode, so that the plain kernels carry
+// none of its code: the single-column decode kernels are sensitive to their
+// instruction footprint (measured: the unexecuted SwiGLU staging in them cost
+// the two-GEMV decode step 2.7 us).
+template <int KIND, int NCMAX, bool SWI>
 __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32, MinBlocks<KIND>::V)
     k_gemv(const __grid_constant__ CUtensorMap tmW, GemvArgs a) {
     using G = SGeo<KIND>;
@@ -1208,7 +1303,7 @@ __global__ void __launch_bounds__((SG<KIND>::NW + 1) * 32, MinBlocks<KIND>::V)
         const Item item = walk.at(i, a, T, rg, NCMAX);
         if (item.e != cur_e || item.col0 != cur_c) {
             if (cur_e >= 0) named_bar_sync(1, NW * 32);   // everyone is done with the old activations
-            stage_x<KIND, NCMAX>(a, T, item, xs, threadIdx.x, NW * 32);
+            stage_x_rows<KIND, NCMAX, SWI>(a, T, item, xs, threadIdx.x, NW * 32);
             named_bar_sync(1, NW * 32);
             if constexpr (XSum<KIND>::ON) {
                 stage_xsum<NCMAX>(xs, xs + NCMAX * K, K, threadIdx.x, NW * 32);
@@ -1264,9 +1359,9 @@ Plan plan(const Problem& p) {
     using G = SGeo<KIND>;
     Plan pl;
     if (p.K > (1 << 24) || p.K % G::UNIT_E) return pl;
-    if (p.row_bytes % 16 || reinterpret_cast<uintptr_t>(p.W) % 16) return pl;
+    if (p.row_bytes % 16 || p.row_stride % 16 || reinterpret_cast<uintptr_t>(p.W) % 16) return pl;
     const bool grouped = p.x_row != nullptr;
-    if (p.x_mode == 1 && (p.x_dtype != 0 || p.K % 4 || p.x_stride % 4 || p.x_stride < 2 * p.K ||
+    if (p.x_mode == 1 && (!p.x_row || p.x_dtype != 0 || p.K % 4 || p.x_stride % 4 || p.x_stride < 2 * p.K ||
                           reinterpret_cast<uintptr_t>(p.X) % 16))
         return pl;
     if (grouped) {
@@ -1337,13 +1432,19 @@ Plan plan(const Problem& p) {
 template <int KIND, int NCMAX>
 cudaError_t launch_nc(const Problem& p, const Plan& pl, cudaStream_t s) {
     using G = SGeo<KIND>;
-    auto kern = k_gemv<KIND, NCMAX>;
+    // SwiGLU staging only for the grouped product (the MoE down projection),
+    // which uses at most four columns per problem
+    auto kern = k_gemv<KIND, NCMAX, false>;
+    if constexpr (NCMAX <= 4) {
+        if (p.x_mode == 1) kern = k_gemv<KIND, NCMAX, true>;
+    }
     // weights as (8-byte word of the row, row, expert)
     CUtensorMap tm;
     const int E = p.x_row ? p.n_experts : 1;
-    const uint64_t estride = p.x_row ? p.expert_stride : static_cast<uint64_t>(p.M) * p.row_bytes;
+    const uint64_t rstride = p.row_stride ? p.row_stride : p.row_bytes;
+    const uint64_t estride = p.x_row ? p.expert_stride : static_cast<uint64_t>(p.M) * rstride;
     const uint64_t dims[3] = {p.row_bytes / 8, static_cast<uint64_t>(p.M), static_cast<uint64_t>(E)};
-    const uint64_t strides[2] = {p.row_bytes, estride};
+    const uint64_t strides[2] = {rstride, estride};
     const uint32_t box[3] = {static_cast<uint32_t>(pl.stride / 8), static_cast<uint32_t>(kRows), 1};
     if (!encode_tiled_map(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, p.W, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE))
@@ -1421,13 +1522,13 @@ void ok_dispatch(const Problem& p, bool* out) { *out = plan<KIND>(p).ok; }
 
 bool gemv_stream_ok(const Problem& p) {
     bool ok = false;
-    QMM_DISPATCH_KIND(p.kind, ok_dispatch, p, &ok);
+    QMM_DISPATCH_GEMV_KIND(p.kind, ok_dispatch, p, &ok);
     return ok;
 }
 
 cudaError_t launch_gemv_stream(const Problem& p, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
-    QMM_DISPATCH_KIND(p.kind, run, p, s, &e);
+    QMM_DISPATCH_GEMV_KIND(p.kind, run, p, s, &e);
     return e;
 }
 

@@ -36,7 +36,8 @@ bool encode_tiled_map(CUtensorMap* tm, CUtensorMapDataType dt, int rank, const v
 struct Problem {
     int kind;
     const uint8_t* W;        // weights (expert 0 for grouped)
-    size_t row_bytes;
+    size_t row_bytes;        // bytes of the K elements a row contributes
+    size_t row_stride = 0;   // bytes between rows (0: row_bytes; a K-slice view is shorter)
     int64_t M, K, N;         // N = columns (plain) or assignments (grouped)
     const void* X;
     int x_dtype;             // 0 f32, 1 f16
@@ -83,9 +84,21 @@ cudaError_t launch_dequant(int kind, const uint8_t* w, int64_t nblocks, float* o
 cudaError_t launch_generic(const Problem& p, cudaStream_t s);
 
 // k_gemv.cu : weight-streaming GEMV (bulk-copy staged rows): N <= 8 columns, or
-// the expert-grouped product (p.x_row set)
+// the expert-grouped product (p.x_row set). p.kind may be a repacked layout.
 bool gemv_stream_ok(const Problem& p);
 cudaError_t launch_gemv_stream(const Problem& p, cudaStream_t s);
+
+// k_repack.cu : the repacked layouts (qrepack) and the split-K GEMV. Problem
+// kind ids of the repacked layouts (decode.cuh Q8_0R / Q4_0R).
+constexpr int kRepackedQ8_0 = 11, kRepackedQ4_0 = 12;
+size_t repack_bytes(int kind, int64_t rows, int64_t cols);
+cudaError_t launch_repack(int kind, const uint8_t* w, int64_t rows, int64_t cols, uint8_t* out, cudaStream_t s);
+// qgemm_repacked: the streaming GEMV over K-slices of a (repacked or native)
+// layout, split ways, with an ordered reduce; split 0 = automatic. Returns a
+// qmm_status.
+int launch_gemv_split(const Problem& p, int split, cudaStream_t s);
+// Frees the split-K path's grown workspaces on every device.
+bool release_split_workspaces();
 
 // k_moe.cu : the mixture-of-experts layer (qmoe_ffn)
 size_t moe_workspace_bytes(int64_t T, int top_k, int64_t d_model, int64_t d_ff);

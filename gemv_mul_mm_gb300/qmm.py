@@ -31,7 +31,7 @@ STATUS = {
 }
 STATUS_ID = {v: k for k, v in STATUS.items()}
 
-PATH_AUTO, PATH_GENERIC, PATH_GEMV, PATH_TC, PATH_DEQUANT, PATH_GROUPED, PATH_MOE = 0, 1, 2, 3, 4, 5, 6
+PATH_AUTO, PATH_GENERIC, PATH_GEMV, PATH_TC, PATH_DEQUANT, PATH_GROUPED, PATH_MOE, PATH_REPACKED = range(8)
 FLAG_WEIGHTS_CONST = 1
 FLAG_Y_F16 = 2
 FLAG_Y_BF16 = 4
@@ -68,6 +68,10 @@ def _lib():
         L.qgemm_noalloc.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _I64, _P]
         L.qgemm_grouped.argtypes = [_I, _P, _SZ, _SZ, _I, _P, _I, _SZ, _I64, _P, _P, _I64,
                                     _P, _SZ, _I64, _I64, _P]
+        L.qrepack.argtypes = [_I, _P, _SZ, _I64, _I64, _P, _SZ, _P]
+        L.qrepack_bytes.argtypes = [_I, _I64, _I64]
+        L.qrepack_bytes.restype = _SZ
+        L.qgemm_repacked.argtypes = [_I, _P, _SZ, _P, _I, _SZ, _P, _SZ, _I64, _I64, _I64, _I, ctypes.c_uint32, _P]
         L.qmoe_ffn.argtypes = [_I, _P, _SZ, _SZ, _P, _SZ, _SZ, _I, _P, _SZ, _I64, _I64, _I64, _P, _P, _I,
                                _P, _SZ, _P, _SZ, _P]
         L.qmoe_ffn_workspace_bytes.argtypes = [_I64, _I, _I64, _I64]
@@ -220,6 +224,33 @@ def qgemm_grouped(kind, W, expert_stride: int, n_experts: int, X, x_row, expert_
                                 n_experts, _ptr(X), _xdt(X), X.numel(), n_x_rows, _ptr(x_row),
                                 _ptr(expert_id), n_assign, _ptr(Y), Y.numel(), M, K,
                                 _stream(stream)), "qgemm_grouped")
+    return Y
+
+
+def qrepack_bytes(kind, rows: int, cols: int) -> int:
+    return _lib().qrepack_bytes(_kind(kind), rows, cols)
+
+
+def qrepack(kind, W, rows: int, cols: int, out=None, stream=None):
+    """The repacked (structure-of-arrays) copy of Q8_0 / Q4_0 weights, as a
+    CUDA uint8 tensor of the same size."""
+    import torch
+    if out is None:
+        out = torch.empty(max(1, qrepack_bytes(kind, rows, cols)), dtype=torch.uint8, device=W.device)
+    _check(_lib().qrepack(_kind(kind), _ptr(W), W.numel() * W.element_size(), rows, cols, _ptr(out), out.numel(),
+                          _stream(stream)), "qrepack")
+    return out
+
+
+def qgemm_repacked(kind, R, X, M: int, K: int, N: int, Y=None, split: int = 0, stream=None,
+                   weights_const: bool = False, out_dtype=None):
+    """qgemm (N <= 8) on a repacked tensor, K split `split` ways (0 = automatic)."""
+    import torch
+    if Y is None:
+        Y = torch.empty((N, M), dtype=out_dtype or torch.float32, device=R.device)
+    flags = (FLAG_WEIGHTS_CONST if weights_const else 0) | _yflag(Y)
+    _check(_lib().qgemm_repacked(_kind(kind), _ptr(R), R.numel(), _ptr(X), _xdt(X), X.numel(), _ptr(Y), Y.numel(),
+                                 M, K, N, split, flags, _stream(stream)), "qgemm_repacked")
     return Y
 
 

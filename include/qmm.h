@@ -265,6 +265,44 @@ QMM_API int qgemm_grouped(int kind, const void* W, size_t w_bytes, size_t expert
                   float* Y, size_t y_elems, int64_t M, int64_t K, void* stream);
 
 /*
+ * qrepack -- load-time repack of Q8_0 / Q4_0 weights into the layout
+ * qgemm_repacked reads (the Vulkore examples/llm/quant_test.cpp page's
+ * repacked fast path: scales split from codes, everything aligned, checked to
+ * reconstruct every element bit-exactly). Rows stay contiguous and keep their
+ * byte count; each 256-element unit of a row holds the code fields of its
+ * eight blocks back to back (16 bytes per Q4_0 block, 32 per Q8_0 block, in
+ * the block's own element order), then the eight f16 scales (16 bytes).
+ *
+ *   W, w_bytes     device, rows x cols native blocks
+ *   out, out_bytes device, qrepack_bytes(kind, rows, cols) bytes (the same
+ *                  size as the native tensor); any alignment for W and out,
+ *                  16 bytes for qgemm_repacked
+ * cols must be a multiple of 256; other kinds are QMM_ERR_UNIMPLEMENTED.
+ */
+QMM_API int qrepack(int kind, const void* W, size_t w_bytes, int64_t rows, int64_t cols, void* out,
+                    size_t out_bytes, void* stream);
+
+/* Bytes of the repacked tensor (0 for an unsupported kind or shape). */
+QMM_API size_t qrepack_bytes(int kind, int64_t rows, int64_t cols);
+
+/*
+ * qgemm_repacked -- qgemm (N <= 8 activation rows) on a tensor repacked by
+ * qrepack, with the reduction over K optionally split: split ways of K / split
+ * elements each (split a divisor of K / 256; 0 = chosen so that every SM gets
+ * about two items of rows; 1 = not split). Each K-slice of every row is
+ * streamed by its own CTA work item and the partial products are added by a
+ * second kernel in slice order (deterministic), the split-k matvec plus
+ * reduce of the same page. flags as qgemm_ex.
+ *
+ * Scratch for split > 1 (the partial products, split * N * M fp32) lives in a
+ * per-device workspace the library grows on demand; growth during stream
+ * capture is refused (QMM_ERR_WORKSPACE_IN_CAPTURE), qmm_shutdown frees it.
+ */
+QMM_API int qgemm_repacked(int kind, const void* R, size_t r_bytes, const void* X, int x_dtype, size_t x_elems,
+                           float* Y, size_t y_elems, int64_t M, int64_t K, int64_t N, int split, uint32_t flags,
+                           void* stream);
+
+/*
  * qmoe_ffn -- one mixture-of-experts feed-forward layer over block-quantized
  * experts (the decoder layer whose per-token weight traffic the inferencelayer
  * 0.2.8 src/cublas_prefill.rs page quotes for Qwen3-30B-A3B). For token t and
@@ -338,7 +376,7 @@ QMM_API int qmm_set_path(int path);
 
 /* Which kernel family the most recent successful call on this host thread
  * launched: 1 generic, 2 streaming GEMV, 3 tensor-core GEMM, 4 dequant,
- * 5 grouped GEMV, 6 MoE layer; 0 before any call. */
+ * 5 grouped GEMV, 6 MoE layer, 7 repacked (split-K) GEMV; 0 before any call. */
 QMM_API int qmm_last_path(void);
 
 /* Number of kernels this library has launched since load (all threads). */
