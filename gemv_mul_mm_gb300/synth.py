@@ -25,7 +25,7 @@ from __future__ import annotations
 import numpy as np
 
 KINDS = ["Q8_0", "Q4_0", "Q5_0", "Q4_K", "Q5_K", "Q6_K",
-         "Q2_K", "Q3_K", "IQ4_NL", "IQ4_XS", "MXFP4"]
+         "Q2_K", "Q3_K", "IQ4_NL", "IQ4_XS", "MXFP4", "Q4_1", "Q5_1", "Q8_1"]
 KIND_INDEX = {k: i for i, k in enumerate(KINDS)}
 
 # (block bytes, block elements, byte offsets of the f16 scale fields)
@@ -41,6 +41,9 @@ _LAYOUT = {
     "IQ4_NL": (18, 32, (0,)),
     "IQ4_XS": (136, 256, (0,)),
     "MXFP4": (17, 32, ()),
+    "Q4_1": (20, 32, (0, 2)),
+    "Q5_1": (24, 32, (0, 2)),
+    "Q8_1": (36, 32, (0,)),   # the f16 at byte 2 stays random: no element reads it
 }
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)

@@ -23,7 +23,7 @@ from typing import Optional
 import numpy as np
 
 KINDS = ["Q8_0", "Q4_0", "Q5_0", "Q4_K", "Q5_K", "Q6_K",
-         "Q2_K", "Q3_K", "IQ4_NL", "IQ4_XS", "MXFP4"]
+         "Q2_K", "Q3_K", "IQ4_NL", "IQ4_XS", "MXFP4", "Q4_1", "Q5_1", "Q8_1"]
 KIND_ID = {k: i for i, k in enumerate(KINDS)}
 PARITY_UNPINNED = ("Q5_K", "Q2_K", "Q3_K")
 

@@ -38,6 +38,16 @@
  *                             four bits; codes carry a -8 bias).
  *   IQ4_NL, IQ4_XS, MXFP4     ferrox-cuda codebook.rs, the three kind rows and
  *                             the `KVALUES_IQ4NL` / `KVALUES_MXFP4` tables.
+ *   Q4_1, Q5_1, Q8_1          named by ferrox-cuda 0.21.0 mul_mm.rs (the
+ *                             `kind_by_name` test's list of kinds with no
+ *                             kernel) without a layout; this file takes the
+ *                             public GGUF block definitions: Q4_1 and Q5_1 are
+ *                             Q4_0 and Q5_0 with unsigned codes and an f16
+ *                             min after the f16 scale (w = d*q + m); Q8_1 is
+ *                             Q8_0 with an f16 field after d that holds d times
+ *                             the sum of the codes, which no element reads
+ *                             (w = d*q). PARITY UNPINNED against the pages
+ *                             for these three, as for the next three.
  *   Q5_K, Q2_K, Q3_K          named by ferrox-cuda mul_mm.rs (module docs and
  *                             `KINDS`), which also says Q5_K shares Q4_K's
  *                             6-bit scale/min unpack and that Q3_K has an
@@ -69,12 +79,13 @@
 /* Format identifiers of the oracle (its own numbering, by name in Python). */
 enum {
     OR_Q8_0 = 0, OR_Q4_0, OR_Q5_0, OR_Q4_K, OR_Q5_K, OR_Q6_K,
-    OR_Q2_K, OR_Q3_K, OR_IQ4_NL, OR_IQ4_XS, OR_MXFP4, OR_NKINDS
+    OR_Q2_K, OR_Q3_K, OR_IQ4_NL, OR_IQ4_XS, OR_MXFP4,
+    OR_Q4_1, OR_Q5_1, OR_Q8_1, OR_NKINDS
 };
 
 /* Bytes and elements of one block, per format. */
-static const int kBlockBytes[OR_NKINDS] = {34, 18, 22, 144, 176, 210, 84, 110, 18, 136, 17};
-static const int kBlockElems[OR_NKINDS] = {32, 32, 32, 256, 256, 256, 256, 256, 32, 256, 32};
+static const int kBlockBytes[OR_NKINDS] = {34, 18, 22, 144, 176, 210, 84, 110, 18, 136, 17, 20, 24, 36};
+static const int kBlockElems[OR_NKINDS] = {32, 32, 32, 256, 256, 256, 256, 256, 32, 256, 32, 32, 32, 32};
 
 /* IQ4_NL / IQ4_XS codebook, as printed in ferrox-cuda codebook.rs KVALUES_IQ4NL. */
 static const float kIq4nl[16] = {-127.f, -104.f, -83.f, -65.f, -49.f, -35.f, -22.f, -10.f,
@@ -267,6 +278,36 @@ static float block_elem(int kind, const uint8_t* b, int e) {
          * w = 2^(e-127) * E2M1[c]. */
         const int c = e < 16 ? nib(b[1 + e], 0) : nib(b[1 + e - 16], 1);
         return oracle_e8m0(b[0]) * kE2m1[c];
+    }
+    case OR_Q4_1: {
+        /* GGUF reading. 20 B: f16 d, f16 m, 16 B of nibbles packed as Q4_0.
+         * Unsigned code, w = d * q + m (the product is exact; one rounding at
+         * the addition). */
+        const int q = e < 16 ? nib(b[4 + e], 0) : nib(b[4 + e - 16], 1);
+        const float d = oracle_f16((uint16_t)u16le(b, 0));
+        const float m = oracle_f16((uint16_t)u16le(b, 2));
+#if ORACLE_SABOTAGE == 9
+        return d * (float)q - m;
+#else
+        return d * (float)q + m;
+#endif
+    }
+    case OR_Q5_1: {
+        /* GGUF reading. 24 B: f16 d, f16 m, u32 qh, 16 B of nibbles; the fifth
+         * bit of element e is bit e of qh, as in Q5_0. w = d * q + m. */
+        const uint32_t qh = u32le(b, 4);
+        const int lo = nib(b[8 + e % 16], e >= 16);
+        const int q = lo | (int)(((qh >> e) & 1) << 4);
+        return oracle_f16((uint16_t)u16le(b, 0)) * (float)q + oracle_f16((uint16_t)u16le(b, 2));
+    }
+    case OR_Q8_1: {
+        /* GGUF reading. 36 B: f16 d, f16 s (= d * sum of the codes; read by
+         * nothing here), 32 x int8. w = d * q. */
+#if ORACLE_SABOTAGE == 10
+        return oracle_f16((uint16_t)u16le(b, 0)) * (float)s8(b[2 + e]);
+#else
+        return oracle_f16((uint16_t)u16le(b, 0)) * (float)s8(b[4 + e]);
+#endif
     }
     default:
         return NAN;

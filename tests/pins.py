@@ -17,9 +17,11 @@ import numpy as np
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 ONE = (0x00, 0x3C)          # f16 1.0, little-endian
 BLOCK = {"Q8_0": 34, "Q4_0": 18, "Q5_0": 22, "Q4_K": 144, "Q5_K": 176, "Q6_K": 210,
-         "Q2_K": 84, "Q3_K": 110, "IQ4_NL": 18, "IQ4_XS": 136, "MXFP4": 17}
+         "Q2_K": 84, "Q3_K": 110, "IQ4_NL": 18, "IQ4_XS": 136, "MXFP4": 17,
+         "Q4_1": 20, "Q5_1": 24, "Q8_1": 36}
 ELEMS = {"Q8_0": 32, "Q4_0": 32, "Q5_0": 32, "Q4_K": 256, "Q5_K": 256, "Q6_K": 256,
-         "Q2_K": 256, "Q3_K": 256, "IQ4_NL": 32, "IQ4_XS": 256, "MXFP4": 32}
+         "Q2_K": 256, "Q3_K": 256, "IQ4_NL": 32, "IQ4_XS": 256, "MXFP4": 32,
+         "Q4_1": 32, "Q5_1": 32, "Q8_1": 32}
 
 
 def load_table(name):
@@ -203,6 +205,109 @@ def check_q5_0_qh(orc):
     want = [-16.0] * 32
     want[3], want[19] = -9.0, -6.0
     return bad + _diff("q5_0 nibbles", decode(orc, "Q5_0", b), want)
+
+
+# ---------------------------------------------------------------------------
+# the kinds with no mul_mm kernel on the pages (GGUF reading): Q4_1, Q5_1, Q8_1
+# ---------------------------------------------------------------------------
+F16_MINUS_8 = 0xC800       # -8.0
+F16_MINUS_16 = 0xCC00      # -16.0
+F16_60000 = 0x7B53         # 60000.0
+F16_TINY = 0x0401          # 2^-14 * (1 + 2^-10), the smallest normal f16 plus one ulp
+
+
+def check_q4_1(orc):
+    """Q4_1 = Q4_0's nibble packing with unsigned codes plus an f16 min after
+    d: with d = 1, m = 0 and byte j = j | (15 - j) << 4, element j is j and
+    element j + 16 is 15 - j. With m = -8 (d = 1) every element is Q4_0's
+    value of the same code bytes, j - 8 and 7 - j. With d = 0 every element
+    is m. d*q + m rounds once: d = 2^-14 (1 + 2^-10), q = 15, m = 60000 gives
+    60000 exactly (the product is far below half an fp32 ulp of 60000)."""
+    bad = []
+    b = blk("Q4_1")
+    b[0], b[1] = ONE
+    for j in range(16):
+        b[4 + j] = j | ((15 - j) << 4)
+    bad += _diff("q4_1 codes", decode(orc, "Q4_1", b), [j for j in range(16)] + [15 - j for j in range(16)])
+    put16(b, 2, F16_MINUS_8)
+    bad += _diff("q4_1 m = -8", decode(orc, "Q4_1", b), [j - 8 for j in range(16)] + [7 - j for j in range(16)])
+    b0 = blk("Q4_1")
+    put16(b0, 2, 0x3E00)   # m = 1.5, d = 0
+    b0[4:20] = 0xFF
+    bad += _diff("q4_1 d = 0", decode(orc, "Q4_1", b0), [1.5] * 32)
+    b1 = blk("Q4_1")
+    put16(b1, 0, F16_TINY)
+    put16(b1, 2, F16_60000)
+    b1[4:20] = 0xFF
+    bad += _diff("q4_1 rounds once", decode(orc, "Q4_1", b1), [60000.0] * 32)
+    return bad
+
+
+def check_q5_1(orc):
+    """Q5_1 = Q5_0's bit layout after an f16 min, unsigned codes: with d = 1,
+    m = 0 and zero nibbles every element is 0 except the one whose qh bit is
+    set, which is 16; with m = -16 it reduces to Q5_0 (-16 everywhere, 0
+    where the bit is set); the nibble order is Q4_0's."""
+    bad = []
+    for e0 in (0, 7, 15, 16, 23, 31):
+        b = blk("Q5_1")
+        b[0], b[1] = ONE
+        qh = 1 << e0
+        b[4:8] = [qh & 0xFF, (qh >> 8) & 0xFF, (qh >> 16) & 0xFF, (qh >> 24) & 0xFF]
+        want = [0.0] * 32
+        want[e0] = 16.0
+        bad += _diff(f"q5_1 qh bit {e0}", decode(orc, "Q5_1", b), want)
+        put16(b, 2, F16_MINUS_16)
+        want = [-16.0] * 32
+        want[e0] = 0.0
+        bad += _diff(f"q5_1 qh bit {e0}, m = -16", decode(orc, "Q5_1", b), want)
+    b = blk("Q5_1")
+    b[0], b[1] = ONE
+    b[8 + 3] = 0xA7
+    want = [0.0] * 32
+    want[3], want[19] = 7.0, 10.0
+    return bad + _diff("q5_1 nibbles", decode(orc, "Q5_1", b), want)
+
+
+def check_q8_1(orc):
+    """Q8_1 = Q8_0's int8 codes after an extra f16 field (d times the code sum),
+    which no element reads: the codes of check_q8_0 at byte 4 give the same
+    values whatever the field holds (0, a NaN, an infinity)."""
+    bad = []
+    codes = [0x00, 0x7F, 0x80, 0xFF, 0x01, 0x81, 0x40, 0xC0] * 4
+    want = [0, 127, -128, -1, 1, -127, 64, -64] * 4
+    for sfield in (0x0000, 0x7E00, 0x7C00, 0x3C00):
+        b = blk("Q8_1")
+        b[0], b[1] = ONE
+        put16(b, 2, sfield)
+        b[4:36] = codes
+        bad += _diff(f"q8_1 s = {sfield:#06x}", decode(orc, "Q8_1", b), want)
+    return bad
+
+
+def check_legacy_min_formats_reduce(orc):
+    """Cross-format invariants on random blocks: Q4_1 with m = -8 d is Q4_0,
+    Q5_1 with m = -16 d is Q5_0, Q8_1 is Q8_0 (same d and code bytes). d is a
+    power of two so that -8 d and -16 d are exact f16 values."""
+    bad = []
+    rng = np.random.default_rng(7)
+    for _ in range(64):
+        e = int(rng.integers(-10, 4))
+        d_bits = (15 + e) << 10                      # 2^e
+        codes = rng.integers(0, 256, 32, dtype=np.uint8)
+        qh = rng.integers(0, 256, 4, dtype=np.uint8)
+        q40 = blk("Q4_0"); put16(q40, 0, d_bits); q40[2:18] = codes[:16]
+        q41 = blk("Q4_1"); put16(q41, 0, d_bits); put16(q41, 2, 0x8000 | ((18 + e) << 10)); q41[4:20] = codes[:16]
+        bad += _diff("q4_1 vs q4_0", decode(orc, "Q4_1", q41), decode(orc, "Q4_0", q40))
+        q50 = blk("Q5_0"); put16(q50, 0, d_bits); q50[2:6] = qh; q50[6:22] = codes[:16]
+        q51 = blk("Q5_1"); put16(q51, 0, d_bits); put16(q51, 2, 0x8000 | ((19 + e) << 10))
+        q51[4:8] = qh; q51[8:24] = codes[:16]
+        bad += _diff("q5_1 vs q5_0", decode(orc, "Q5_1", q51), decode(orc, "Q5_0", q50))
+        q80 = blk("Q8_0"); put16(q80, 0, d_bits); q80[2:34] = codes
+        q81 = blk("Q8_1"); put16(q81, 0, d_bits); q81[2:4] = rng.integers(0, 256, 2, dtype=np.uint8)
+        q81[4:36] = codes
+        bad += _diff("q8_1 vs q8_0", decode(orc, "Q8_1", q81), decode(orc, "Q8_0", q80))
+    return bad
 
 
 # ---------------------------------------------------------------------------
@@ -469,7 +574,7 @@ def check_gemm_brute_force(orc):
         for r in range(M):                 # keep f16 scale fields finite and small
             o = r * BLOCK[kind]
             for off in {"Q6_K": (208,), "Q2_K": (80, 82), "Q3_K": (108,),
-                        "MXFP4": ()}.get(kind, (0, 2) if kind in ("Q4_K", "Q5_K") else (0,)):
+                        "MXFP4": ()}.get(kind, (0, 2) if kind in ("Q4_K", "Q5_K", "Q4_1", "Q5_1") else (0,)):
                 put16(w, o + off, 0x2000 + int(rng.integers(0, 0x400)))
             if kind == "MXFP4":
                 w[o] = 120 + int(rng.integers(0, 8))

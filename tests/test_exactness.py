@@ -2,7 +2,8 @@
 
 Every element of every format is a product of an fp32 block scale, an integer
 sub-scale and an integer code (or a codebook value), minus, for the affine-min
-formats (Q4_K, Q5_K, Q2_K), a second product of a scale and an integer min.
+formats (Q4_K, Q5_K, Q2_K), a second product of a scale and an integer min
+(Q4_1 and Q5_1 add an f16 min instead).
 The significant bits of each product stay within fp32's 24, so the product is
 exact and its association order does not matter; the affine formats round
 once, at the subtraction, which an FMA also does. This is what makes a
@@ -12,7 +13,7 @@ multiply block scales into partial sums instead of operands.
 The check: factors are extracted here, in numpy, straight from the block bytes
 (the byte layouts of the Vulkore `ref::` CPU references for Q8_0, Q5_0, Q4_K
 and Q6_K, the ferrox-cuda codebook.rs page for IQ4_NL, IQ4_XS and MXFP4, the
-GGUF reading for Q5_K, Q2_K and Q3_K); for every element, (a * b) * c,
+GGUF reading for Q5_K, Q2_K, Q3_K, Q4_1, Q5_1 and Q8_1); for every element, (a * b) * c,
 a * (b * c) and the exact product (fp64, where it is exact) must agree
 bitwise, the FMA-contracted affine form must equal the subtract form, and the
 result must equal the oracle's dequant bit for bit.
@@ -120,6 +121,17 @@ def factors(kind, b):
             sh = bi[:, 2] | (bi[:, 3] << 8)
             ls = ((bi[:, 4 + ib // 2] >> (4 * (ib & 1))) & 15) | (((sh >> (2 * ib)) & 3) << 4)
             a[:, e], sub[:, e], q[:, e] = _f16(b, 0), ls - 32, KV_IQ4[c]
+        elif kind == "Q8_1":
+            a[:, e] = _f16(b, 0)
+            q[:, e] = b[:, 4 + e].view(np.int8)
+        elif kind == "Q4_1":
+            # w = d * q + m: the min enters as dmin = -m times mn = 1
+            a[:, e], q[:, e] = _f16(b, 0), _nib(b[:, 4:20], e)
+            dmin[:, e], mn[:, e] = -_f16(b, 2), 1.0
+        elif kind == "Q5_1":
+            qh = bi[:, 4] | (bi[:, 5] << 8) | (bi[:, 6] << 16) | (bi[:, 7] << 24)
+            a[:, e], q[:, e] = _f16(b, 0), _nib(b[:, 8:24], e) | (((qh >> e) & 1) << 4)
+            dmin[:, e], mn[:, e] = -_f16(b, 2), 1.0
         else:
             raise ValueError(kind)
     return a, sub, q, dmin, mn

@@ -13,7 +13,8 @@ PIN_CHECKS = [
     pins.check_iq4nl_codebook, pins.check_e2m1_codebook, pins.check_mxfp4_scale,
     pins.check_q4_0_nibbles, pins.check_q8_0, pins.check_q5_0_qh,
     pins.check_q4_k, pins.check_q5_k, pins.check_q6_k, pins.check_q2_k, pins.check_q3_k,
-    pins.check_iq4_xs, pins.check_gemm_brute_force,
+    pins.check_iq4_xs, pins.check_q4_1, pins.check_q5_1, pins.check_q8_1,
+    pins.check_legacy_min_formats_reduce, pins.check_gemm_brute_force,
 ]
 
 
@@ -33,6 +34,8 @@ SABOTAGE = {
     6: pins.check_q4_k,           # Q4_K min term dropped
     7: pins.check_e2m1_codebook,  # MXFP4 code 8 as +0.0
     8: pins.check_gemm_brute_force,  # activation index transposed inside a pair
+    9: pins.check_q4_1,           # Q4_1 min subtracted instead of added
+    10: pins.check_q8_1,          # Q8_1 codes read from byte 2, as in Q8_0
 }
 
 
@@ -46,7 +49,8 @@ def test_pin_fires_on_sabotage(sab):
 def test_geometry(orc):
     want = {"Q8_0": (34, 32), "Q4_0": (18, 32), "Q5_0": (22, 32), "Q4_K": (144, 256),
             "Q5_K": (176, 256), "Q6_K": (210, 256), "Q2_K": (84, 256), "Q3_K": (110, 256),
-            "IQ4_NL": (18, 32), "IQ4_XS": (136, 256), "MXFP4": (17, 32)}
+            "IQ4_NL": (18, 32), "IQ4_XS": (136, 256), "MXFP4": (17, 32),
+            "Q4_1": (20, 32), "Q5_1": (24, 32), "Q8_1": (36, 32)}
     for k, g in want.items():
         assert orc.geometry(k) == g
 
