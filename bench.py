@@ -430,7 +430,7 @@ def secondary_table(qmm, synth, l2_bytes, stream, pk):
 
     # prefill GEMMs (and the dequant of the same tensors)
     gem = {}
-    for cfg in (synth.KQUANT, synth.CODEBOOK):
+    for cfg in (synth.KQUANT, synth.CODEBOOK, synth.LEGACY1):
         M, K, N = cfg["M"], cfg["K"], cfg["N"]
         xh = synth.workload_x(cfg, cfg["kinds"][0])
         X = torch.from_numpy(xh).cuda()
@@ -741,7 +741,7 @@ def run_case(a):
         x = torch.from_numpy(synth.workload_x(c, arg)).cuda()
         fn = lambda: qmm.qgemv(arg, W, x, c["M"], c["K"], weights_const=True)
     elif what == "gemm":
-        c = synth.KQUANT if arg in synth.KQUANT["kinds"] else synth.CODEBOOK
+        c = next(cf for cf in (synth.KQUANT, synth.CODEBOOK, synth.LEGACY1) if arg in cf["kinds"])
         W = torch.from_numpy(synth.workload_weights(c, arg)).cuda()
         X = torch.from_numpy(synth.workload_x(c, arg)).cuda()
         fn = lambda: qmm.qgemm(arg, W, X, c["M"], c["K"], c["N"])
@@ -752,8 +752,7 @@ def run_case(a):
         xr, eid = torch.from_numpy(p["x_row"]).cuda(), torch.from_numpy(p["expert_id"]).cuda()
         fn = lambda: qmm.qgemm_grouped(p["kind"], W, p["stride"], p["n_experts"], X, xr, eid, p["M"], p["K"])
     elif what == "dequant":
-        c = synth.DECODE if arg in ("Q8_0", "Q4_0") else (synth.KQUANT if arg in synth.KQUANT["kinds"]
-                                                           else synth.CODEBOOK)
+        c = next(cf for cf in (synth.DECODE, synth.KQUANT, synth.CODEBOOK, synth.LEGACY1) if arg in cf["kinds"])
         W = torch.from_numpy(synth.workload_weights(c, arg)).cuda()
         fn = lambda: qmm.qdequant(arg, W, c["M"], c["K"])
     else:

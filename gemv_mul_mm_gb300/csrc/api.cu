@@ -25,7 +25,8 @@ struct KindRow {
 constexpr KindRow kKinds[QMM_NKINDS] = {
     {"Q8_0", 34, 32},   {"Q4_0", 18, 32},   {"Q5_0", 22, 32},    {"Q4_K", 144, 256},
     {"Q5_K", 176, 256}, {"Q6_K", 210, 256}, {"Q2_K", 84, 256},   {"Q3_K", 110, 256},
-    {"IQ4_NL", 18, 32}, {"IQ4_XS", 136, 256}, {"MXFP4", 17, 32},
+    {"IQ4_NL", 18, 32}, {"IQ4_XS", 136, 256}, {"MXFP4", 17, 32}, {"Q4_1", 20, 32},
+    {"Q5_1", 24, 32},   {"Q8_1", 36, 32},
 };
 
 std::atomic<uint64_t> g_launches{0};

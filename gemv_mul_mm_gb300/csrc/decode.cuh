@@ -24,11 +24,12 @@ namespace qmm {
 
 enum Kind : int {
     Q8_0 = 0, Q4_0 = 1, Q5_0 = 2, Q4_K = 3, Q5_K = 4, Q6_K = 5,
-    Q2_K = 6, Q3_K = 7, IQ4_NL = 8, IQ4_XS = 9, MXFP4 = 10, NKINDS = 11,
+    Q2_K = 6, Q3_K = 7, IQ4_NL = 8, IQ4_XS = 9, MXFP4 = 10,
+    Q4_1 = 11, Q5_1 = 12, Q8_1 = 13, NKINDS = 14,
     // Library-internal layouts made by qrepack (not block formats of the ABI):
     // Q8_0 / Q4_0 rows as units of eight blocks, the eight code fields back to
     // back (32 / 16 bytes each) and then the eight f16 scales (16 bytes).
-    Q8_0R = 11, Q4_0R = 12
+    Q8_0R = 32, Q4_0R = 33
 };
 
 template <int KIND> struct Geo;
@@ -43,6 +44,9 @@ template <> struct Geo<Q3_K>   { static constexpr int BB = 110, BE = 256; };
 template <> struct Geo<IQ4_NL> { static constexpr int BB = 18,  BE = 32;  };
 template <> struct Geo<IQ4_XS> { static constexpr int BB = 136, BE = 256; };
 template <> struct Geo<MXFP4>  { static constexpr int BB = 17,  BE = 32;  };
+template <> struct Geo<Q4_1>   { static constexpr int BB = 20,  BE = 32;  };
+template <> struct Geo<Q5_1>   { static constexpr int BB = 24,  BE = 32;  };
+template <> struct Geo<Q8_1>   { static constexpr int BB = 36,  BE = 32;  };
 template <> struct Geo<Q8_0R>  { static constexpr int BB = 34,  BE = 32;  };
 template <> struct Geo<Q4_0R>  { static constexpr int BB = 18,  BE = 32;  };
 
@@ -139,7 +143,16 @@ __device__ __forceinline__ float elem32(const uint8_t* b, int j, int i) {
         const uint32_t sh = ld16(b, 2);
         const int ls = ((b[4 + (j >> 1)] >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4);
         return h2f(ld16(b, 0)) * static_cast<float>(ls - 32) * c_kv_iq4nl[c];
+    } else if constexpr (KIND == Q4_1 || KIND == Q5_1) {
+        constexpr int QS = (KIND == Q5_1) ? 8 : 4;
+        const uint32_t byte = b[QS + (i & 15)];
+        int q = (i < 16) ? (byte & 15) : (byte >> 4);
+        if constexpr (KIND == Q5_1) q |= static_cast<int>((b[4 + (i >> 3)] >> (i & 7)) & 1) << 4;
+        return __fadd_rn(__fmul_rn(h2f(ld16(b, 0)), static_cast<float>(q)), h2f(ld16(b, 2)));
+    } else if constexpr (KIND == Q8_1) {
+        return h2f(ld16(b, 0)) * static_cast<float>(static_cast<int8_t>(b[4 + i]));
     } else {  // MXFP4
+        static_assert(KIND == MXFP4, "every format has an element decoder");
         const uint32_t byte = b[1 + (i & 15)];
         const int c = (i < 16) ? (byte & 15) : (byte >> 4);
         return e8m0f(b[0]) * c_kv_e2m1[c];
@@ -241,7 +254,23 @@ __device__ __forceinline__ float4 elem4(const uint8_t* b, int e, const float* tb
             const uint32_t byte = b[8 + 16 * j + (i & 15)];
             v[t] = ds * tbl[(i < 16) ? (byte & 15) : (byte >> 4)];
         }
+    } else if constexpr (KIND == Q4_1 || KIND == Q5_1) {
+        constexpr int QS = (KIND == Q5_1) ? 8 : 4;
+        const float d = h2f(ld16(b, 0)), m = h2f(ld16(b, 2));
+        const uint32_t qh = (KIND == Q5_1) ? (ld8(b, 4) | (ld8(b, 5) << 8) | (ld8(b, 6) << 16) | (ld8(b, 7) << 24)) : 0u;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int i = i0 + t;
+            const uint32_t byte = b[QS + (i & 15)];
+            const uint32_t q = ((i < 16) ? (byte & 15) : (byte >> 4)) | (((qh >> i) & 1u) << 4);
+            v[t] = __fadd_rn(__fmul_rn(d, static_cast<float>(q)), m);
+        }
+    } else if constexpr (KIND == Q8_1) {
+        const float d = h2f(ld16(b, 0));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[t] = d * static_cast<float>(static_cast<int8_t>(b[4 + i0 + t]));
     } else {  // MXFP4
+        static_assert(KIND == MXFP4, "every format has an element decoder");
         const float s = e8m0f(b[0]);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -270,6 +299,9 @@ __device__ __forceinline__ float codebook_entry(int c) {
 //   Q5_0    q - 16                                   d        per 32
 //   IQ4_NL  KV[c]                                    d        per 32
 //   MXFP4   E2M1[c]                                  2^(e-127) per 32
+//   Q8_1    q                                        d        per 32
+//   Q4_1    q                                        d        per 32;   mins: m (an f16)
+//   Q5_1    q                                        d        per 32;   mins: m (an f16)
 //   Q4_K    sc_j * q            (<= 945)             d per 256;  mins: dmin * m_j
 //   Q5_K    sc_j * q            (<= 1953)            d per 256;  mins: dmin * m_j
 //   Q6_K    sc * (q - 32)       (<= 4096; rounds once above 2048)   d per 256
@@ -279,7 +311,7 @@ __device__ __forceinline__ float codebook_entry(int c) {
 // ---------------------------------------------------------------------------
 template <int KIND> struct TcGeo {
     static constexpr bool PER32 = Geo<KIND>::BE == 32;                       // scale per 32-element block
-    static constexpr bool MINS = KIND == Q4_K || KIND == Q5_K || KIND == Q2_K;
+    static constexpr bool MINS = KIND == Q4_K || KIND == Q5_K || KIND == Q2_K || KIND == Q4_1 || KIND == Q5_1;
     static constexpr int MIN_GROUPS = KIND == Q2_K ? 16 : 8;                 // min groups per 256
 };
 
@@ -325,6 +357,9 @@ __device__ __forceinline__ float2 scale256(const uint8_t* b) {
     case ::qmm::Q3_K: FN<::qmm::Q3_K>(__VA_ARGS__); break;        \
     case ::qmm::IQ4_NL: FN<::qmm::IQ4_NL>(__VA_ARGS__); break;    \
     case ::qmm::IQ4_XS: FN<::qmm::IQ4_XS>(__VA_ARGS__); break;    \
+    case ::qmm::Q4_1: FN<::qmm::Q4_1>(__VA_ARGS__); break;        \
+    case ::qmm::Q5_1: FN<::qmm::Q5_1>(__VA_ARGS__); break;        \
+    case ::qmm::Q8_1: FN<::qmm::Q8_1>(__VA_ARGS__); break;        \
     default: FN<::qmm::MXFP4>(__VA_ARGS__); break;                \
     }
 

@@ -65,12 +65,15 @@ constexpr int kTmemCols = 512;
 // Tensor memory (512 columns x 128 lanes, lane = weight row of the tile):
 //   [0, 128)    A operand: four stages of 64 f16 codes per row (32 columns each)
 //   [128, 512)  fp32 accumulators: three 128-column units, one per 32-element
-//               block, for the per-32 formats; otherwise D1 of two super-blocks
-//               (double buffered) at 128 and 256, and the min term D2 at 384.
+//               block, for the per-32 formats (two, and the min term D2 of the
+//               super-step at 384, for Q4_1 / Q5_1); otherwise D1 of two
+//               super-blocks (double buffered) at 128 and 256, and the min
+//               term D2 at 384.
 constexpr int kAStages = 4;
 constexpr int kACols = KSUB / 2;
 constexpr int kDCol0 = kAStages * kACols;
-template <int KIND> struct NDBuf { static constexpr int N = TcGeo<KIND>::PER32 ? 3 : 2; };
+// (per-32 formats with mins: two units, the min term D2 at column 384)
+template <int KIND> struct NDBuf { static constexpr int N = TcGeo<KIND>::PER32 && !TcGeo<KIND>::MINS ? 3 : 2; };
 // instruction descriptor: D f32, A/B f16, both K-major, N = 128, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
 
@@ -343,12 +346,21 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, unsign
 // with word-wide masks and shifts and made exact f16 by the 0x64 magic byte
 // (1024 + m, minus 1024): Q4_K / Q5_K -- the 8 mins of the 12-byte scale field
 // (bytes 4..7 low 6 bits; bytes 8..11 high nibble with the top 2 bits of bytes
-// 4..7), twice; Q2_K -- the high nibbles of its 16 scale bytes. The row's
-// scale field is 4-byte aligned in the staged tile for all three formats.
+// 4..7), twice; Q2_K -- the high nibbles of its 16 scale bytes; Q4_1 / Q5_1
+// -- the f16 mins of the super-step's eight blocks themselves (bytes 2..3 of
+// each block), twice. The fields are 4-byte aligned in the staged tile.
 template <int KIND>
 __device__ __forceinline__ void min_words(const uint8_t* row, uint32_t (&w)[8]) {
     const uint32_t m1024 = h2int(-1024);
-    if constexpr (KIND == Q2_K) {
+    if constexpr (KIND == Q4_1 || KIND == Q5_1) {
+        constexpr int BW = Geo<KIND>::BB / 4;
+        const uint32_t* f = reinterpret_cast<const uint32_t*>(row);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w[i] = prmt(f[BW * 2 * i], f[BW * (2 * i + 1)], 0x7632u);
+            w[4 + i] = w[i];
+        }
+    } else if constexpr (KIND == Q2_K) {
         const uint32_t* f = reinterpret_cast<const uint32_t*>(row);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -563,6 +575,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_commit(&d_full[ub]);
                         tc_mma_ts(d1, a_tm + 16, xd + 4, kIdesc, 0u);
                         tc_mma_ts(d1, a_tm + 24, xd + 6, kIdesc, 1u);
+                        if constexpr (MN::ON) {
+                            // the super-step's min term, published with its last block
+                            if (q == KSUP / KSUB - 1) {
+                                const int b = s & 1;
+#pragma unroll
+                                for (int t = 0; t < MN::TILES; ++t)
+                                    tc_mma(tmem + kDCol0 + 2 * BN,
+                                           desc_sw32(smem_u32(amin + b * L::MINB + t * MIN_TILE)),
+                                           desc_sw32(smem_u32(bmin + b * L::MINB + t * MIN_TILE)), kIdesc, t);
+                                tc_commit(&amin_empty[b]);
+                                tc_commit(&bmin_empty[b]);
+                            }
+                        }
                         tc_commit(&d_full[b1]);
                     } else {
                         const uint32_t d = tmem + kDCol0 + (s & 1) * BN;
@@ -618,6 +643,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int h = 0; h < 2; ++h) {
                             const int u = 8 * s + 2 * q + h;
                             if (ok && u >= ND) ok = spin_bar(&d_empty[u % ND], ((u / ND) - 1) & 1, abort_flag, a.err);
+                        }
+                        if constexpr (MN::ON) {
+                            // D2 is free here: the epilogue reads it with the previous
+                            // super-step's last block, which it has finished before
+                            // the blocks waited for above
+                            if (q == KSUP / KSUB - 1) {
+                                const int b = s & 1;
+                                if (ok) ok = spin_bar(&amin_full[b], (s >> 1) & 1, abort_flag, a.err);
+                                if (ok) ok = spin_bar(&bmin_full[b], (s >> 1) & 1, abort_flag, a.err);
+                            }
                         }
                     } else {
                         if (ok && q == 0 && s >= 2) ok = spin_bar(&d_empty[s & 1], ((s >> 1) - 1) & 1, abort_flag, a.err);
@@ -766,6 +801,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int i = 0; i < 16; ++i)
                                     acc[c * 8 + i] = __ffma2_rn(d2, make_float2(v[2 * i], v[2 * i + 1]), acc[c * 8 + i]);
+                                if constexpr (MN::ON) {
+                                    // Q4_1 / Q5_1, with the super-step's last block: + the
+                                    // min term sum_b m_b * (activation sum of block b)
+                                    if (j == 7) {
+                                        tmem_ld16(tmem + lane_addr + kDCol0 + 2 * BN + half * 64 + c * 16,
+                                                  *reinterpret_cast<float(*)[16]>(v));
+                                        tmem_ld16(tmem + lane_addr + kDCol0 + 2 * BN + half * 64 + c * 16 + 16,
+                                                  *reinterpret_cast<float(*)[16]>(v + 16));
+                                        tmem_wait_ld();
+#pragma unroll
+                                        for (int i = 0; i < 16; ++i)
+                                            acc[c * 8 + i] = __fadd2_rn(acc[c * 8 + i], make_float2(v[2 * i], v[2 * i + 1]));
+                                    }
+                                }
                             }
                         }
                         tc_fence_before();

@@ -92,6 +92,9 @@ template <> struct SG<Q6_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; 
 template <> struct SG<Q2_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
 template <> struct SG<Q3_K>   { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
 template <> struct SG<IQ4_XS> { static constexpr int UB = 1,  NW = 8,  NWU = 4; };
+template <> struct SG<Q4_1>   { static constexpr int UB = 8,  NW = 8,  NWU = 2; };
+template <> struct SG<Q5_1>   { static constexpr int UB = 8,  NW = 8,  NWU = 2; };
+template <> struct SG<Q8_1>   { static constexpr int UB = 8,  NW = 8,  NWU = 4; };
 template <> struct SG<Q8_0R>  { static constexpr int UB = 8,  NW = 8,  NWU = 4; };
 template <> struct SG<Q4_0R>  { static constexpr int UB = 8,  NW = 16, NWU = 8; };
 
@@ -190,7 +193,9 @@ __host__ __device__ __forceinline__ int q4_pow(int i) {
 }
 
 // Formats whose minimum term needs the activation sums of each 16-element group.
-template <int KIND> struct XSum { static constexpr bool ON = KIND == Q4_K || KIND == Q5_K || KIND == Q2_K; };
+template <int KIND> struct XSum {
+    static constexpr bool ON = KIND == Q4_K || KIND == Q5_K || KIND == Q2_K || KIND == Q4_1 || KIND == Q5_1;
+};
 
 // Codebook formats (IQ4_NL, IQ4_XS, MXFP4) stage the activations of each
 // 32-element group in the order their decoder meets the elements: a code word
@@ -462,6 +467,64 @@ __device__ __forceinline__ void unit_q5_0(const uint8_t* u, const float* xs, int
             }
 #pragma unroll
             for (int n = 0; n < NC; ++n) acc[n] = fmaf(d, S[n].x + S[n].y, acc[n]);
+        }
+    }
+}
+
+// Q4_1 (20 B), Q5_1 (24 B) and Q8_1 (36 B) keep every field 4-byte aligned:
+// four blocks are 80 / 96 / 144 bytes, whole 16-byte vectors from the
+// 16-byte aligned unit. Block scale d on the partial sum; Q4_1 / Q5_1 add
+// their f16 min times the block's activation sum (two per-16 sums).
+template <int KIND, int NC>
+__device__ __forceinline__ void unit_legacy1(const uint8_t* u, const float* xs, const float* xsum, int K, int k0,
+                                             float (&acc)[NC]) {
+    constexpr int BW = Geo<KIND>::BB / 4;   // words per block: 5, 6 or 9
+    const float2 nb = nbias(KIND == Q8_1 ? 128.f : 0.f);
+#pragma unroll 1
+    for (int qd = 0; qd < 2; ++qd) {
+        uint32_t w[4 * BW];
+#pragma unroll
+        for (int i = 0; i < BW; ++i) {
+            const uint4 v = reinterpret_cast<const uint4*>(u + 16 * BW * qd)[i];
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi) {
+            const uint32_t* bw = w + BW * bi;
+            const float d = h2f(bw[0]);
+            const int kb = k0 + 32 * (4 * qd + bi);
+            float2 S[NC];
+            zero2(S);
+            if constexpr (KIND == Q8_1) {
+#pragma unroll
+                for (int wi = 0; wi < 8; ++wi) dot4<NC>(bw[1 + wi] ^ 0x80808080u, nb, xs + kb + 4 * wi, K, S);
+            } else {
+                constexpr int QS = (KIND == Q5_1) ? 2 : 1;   // first code word
+#pragma unroll
+                for (int wi = 0; wi < 4; ++wi) {
+                    uint32_t lo = bw[QS + wi] & 0x0F0F0F0Fu, hi = (bw[QS + wi] >> 4) & 0x0F0F0F0Fu;
+                    if constexpr (KIND == Q5_1) {
+                        lo |= bit4_to_bytes((bw[1] >> (4 * wi)) & 0xFu);
+                        hi |= bit4_to_bytes((bw[1] >> (16 + 4 * wi)) & 0xFu);
+                    }
+                    dot4<NC>(lo, nb, xs + kb + 4 * wi, K, S);
+                    dot4<NC>(hi, nb, xs + kb + 16 + 4 * wi, K, S);
+                }
+            }
+            if constexpr (KIND == Q8_1) {
+#pragma unroll
+                for (int n = 0; n < NC; ++n) acc[n] = fmaf(d, S[n].x + S[n].y, acc[n]);
+            } else {
+                const float m = h2f(bw[0] >> 16);
+#pragma unroll
+                for (int n = 0; n < NC; ++n) {
+                    const float* xsn = xsum + n * (K >> 4) + (kb >> 4);
+                    acc[n] = fmaf(m, xsn[0] + xsn[1], fmaf(d, S[n].x + S[n].y, acc[n]));
+                }
+            }
         }
     }
 }
@@ -835,6 +898,9 @@ __device__ __forceinline__ void unit(const uint8_t* u, const float* xs, const fl
         unit_q2k<NC>(u, xs, xsum, K, k0, acc);
     } else if constexpr (KIND == Q3_K) {
         unit_q3k<NC>(u, xs, K, k0, acc);
+    } else if constexpr (KIND == Q4_1 || KIND == Q5_1 || KIND == Q8_1) {
+        static_assert(SG<KIND>::UB == 8, "the Q4_1 / Q5_1 / Q8_1 decoder takes eight blocks");
+        unit_legacy1<KIND, NC>(u, xs, xsum, K, k0, acc);
     } else {
         static_assert(KIND == IQ4_XS, "every format has a unit decoder");
         unit_iq4xs<NC>(u, xs, K, k0, acc);

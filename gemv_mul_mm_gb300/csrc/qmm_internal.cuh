@@ -90,7 +90,7 @@ cudaError_t launch_gemv_stream(const Problem& p, cudaStream_t s);
 
 // k_repack.cu : the repacked layouts (qrepack) and the split-K GEMV. Problem
 // kind ids of the repacked layouts (decode.cuh Q8_0R / Q4_0R).
-constexpr int kRepackedQ8_0 = 11, kRepackedQ4_0 = 12;
+constexpr int kRepackedQ8_0 = 32, kRepackedQ4_0 = 33;
 size_t repack_bytes(int kind, int64_t rows, int64_t cols);
 cudaError_t launch_repack(int kind, const uint8_t* w, int64_t rows, int64_t cols, uint8_t* out, cudaStream_t s);
 // qgemm_repacked: the streaming GEMV over K-slices of a (repacked or native)

@@ -221,6 +221,70 @@ template <> struct FastDec<Q5_0> {
     }
 };
 
+// Q8_1: Q8_0's codes after a 4-byte head (d and an unread f16), 36-byte blocks
+// (every field 4-byte aligned).
+template <> struct FastDec<Q8_1> {
+    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            uint32_t w[8];
+            ld_words<8, 4>(row + (2 * q + hb) * 36 + 4, w);
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) {
+                const uint32_t u = w[wi] ^ 0x80808080u;
+                o[16 * hb + 2 * wi] = hadd2_u(prmt(u, kMagB, 0x4140), h2int(-1152));
+                o[16 * hb + 2 * wi + 1] = hadd2_u(prmt(u, kMagB, 0x4342), h2int(-1152));
+            }
+        }
+    }
+};
+
+// Q4_1 (20-byte blocks, codes at byte 4) and Q5_1 (24-byte blocks, qh at byte
+// 4, codes at byte 8): Q4_0's and Q5_0's unpack with unsigned codes (no bias);
+// the min term comes from the min MMA, the scale d from the epilogue.
+template <> struct FastDec<Q4_1> {
+    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            uint32_t w[4];
+            ld_words<4, 4>(row + (2 * q + hb) * 20 + 4, w);
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+                const uint32_t t01 = prmt(w[wi], 0u, 0x4140), t23 = prmt(w[wi], 0u, 0x4342);
+                // low nibble: 1024 + n - 1024; high: (1024 + 16 n) / 16 - 64
+                o[16 * hb + 2 * wi] = hadd2_u(lop_and_or(t01, 0x000F000Fu, kMag16), h2int(-1024));
+                o[16 * hb + 2 * wi + 1] = hadd2_u(lop_and_or(t23, 0x000F000Fu, kMag16), h2int(-1024));
+                o[16 * hb + 8 + 2 * wi] = hfma2_u(lop_and_or(t01, 0x00F000F0u, kMag16), kH2Sixteenth, h2int(-64));
+                o[16 * hb + 9 + 2 * wi] = hfma2_u(lop_and_or(t23, 0x00F000F0u, kMag16), kH2Sixteenth, h2int(-64));
+            }
+        }
+    }
+};
+
+template <> struct FastDec<Q5_1> {
+    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            uint32_t w[5];   // qh, then the 16 nibble bytes
+            ld_words<5, 4>(row + (2 * q + hb) * 24 + 4, w);
+            const uint32_t qh = w[0];
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+                const uint32_t t01 = prmt(w[1 + wi], 0u, 0x4140), t23 = prmt(w[1 + wi], 0u, 0x4342);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const uint32_t t = p ? t23 : t01;
+                    const int e = 4 * wi + 2 * p;
+                    const uint32_t ml = lop_and_or(((qh >> e) & 3u) * 0x00080010u, 0x00100010u, kMag16);
+                    const uint32_t mh = lop_and_or(((qh >> (16 + e)) & 3u) * 0x00800100u, 0x01000100u, kMag16);
+                    o[16 * hb + e / 2] = hadd2_u(lop_and_or(t, 0x000F000Fu, ml), h2int(-1024));
+                    o[16 * hb + 8 + e / 2] = hfma2_u(lop_and_or(t, 0x00F000F0u, mh), kH2Sixteenth, h2int(-64));
+                }
+            }
+        }
+    }
+};
+
 // Codebook formats with one 16-byte nibble field per 32 elements.
 template <typename T, uint32_t MAGB, uint32_t BIAS>
 __device__ __forceinline__ void lut_block(const uint32_t (&w)[4], uint32_t scale, uint32_t bias, bool scaled,

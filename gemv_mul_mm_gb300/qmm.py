@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libqmm.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "qmm.h")
 
 KINDS = ["Q8_0", "Q4_0", "Q5_0", "Q4_K", "Q5_K", "Q6_K",
-         "Q2_K", "Q3_K", "IQ4_NL", "IQ4_XS", "MXFP4"]
+         "Q2_K", "Q3_K", "IQ4_NL", "IQ4_XS", "MXFP4", "Q4_1", "Q5_1", "Q8_1"]
 KIND_ID = {k: i for i, k in enumerate(KINDS)}
 F32, F16 = 0, 1
 

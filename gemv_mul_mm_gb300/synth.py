@@ -17,6 +17,8 @@ Workloads (shapes and distributions of the pages' benchmarks):
                               f16 scale fields ~ U[1e-4,1e-2]
   * codebook GEMM             M=11008, K=4096, N=128, f16 X ~ N(0,1); IQ4_NL/IQ4_XS
                               d ~ U[1e-3,1e-2]; MXFP4 E8M0 ~ U{118..130}
+  * Q4_1 / Q5_1 / Q8_1 GEMM   the codebook shape (no workload on the pages), f16 X,
+                              d and m ~ U[1e-3,1e-2]
   * MoE expert-grouped Q4_0   128 experts, gate_up 1536x2048, down 2048x768,
                               T in {1, 8, 64} tokens, 8 distinct experts per token
 """
@@ -208,6 +210,9 @@ KQUANT = dict(config=2, kinds=("Q4_K", "Q5_K", "Q6_K", "Q2_K", "Q3_K"),
               M=4096, K=4096, N=512, x_dtype="f16", scale_lo=1e-4, scale_hi=1e-2)
 CODEBOOK = dict(config=3, kinds=("IQ4_NL", "IQ4_XS", "MXFP4"),
                 M=11008, K=4096, N=128, x_dtype="f16")
+# Q4_1 / Q5_1 / Q8_1 have no workload on the pages: their GEMM tests take the
+# codebook workload's shape.
+LEGACY1 = dict(config=5, kinds=("Q4_1", "Q5_1", "Q8_1"), M=11008, K=4096, N=128, x_dtype="f16")
 MOE = dict(config=4, kind="Q4_0", n_experts=128, top_k=8, d_model=2048, d_ff=768,
            tokens=(1, 8, 64), x_dtype="f32")
 

@@ -54,7 +54,12 @@ extern "C" {
  *   Q6_K 210/256, Q2_K 84/256, Q3_K 110/256, IQ4_NL 18/32, IQ4_XS 136/256,
  *   MXFP4 17/32 (ferrox-cuda mul_mm.rs `KINDS` and its geometry test;
  *   ferrox-cuda 0.20.0 src/mul_mm_kinds/codebook.rs for the codebook rows;
- *   Vulkore examples/llm/quant_test.cpp `kFormats`). */
+ *   Vulkore examples/llm/quant_test.cpp `kFormats`);
+ *   Q4_1 20/32, Q5_1 24/32, Q8_1 36/32: the kinds that ferrox-cuda 0.21.0
+ *   mul_mm.rs lists as having no mul_mm kernel, in the public GGUF layouts --
+ *   Q4_1 and Q5_1 are Q4_0 and Q5_0 with unsigned codes and an f16 min after
+ *   the f16 scale (w = d*q + m); Q8_1 is Q8_0 with an f16 field after d (d
+ *   times the sum of the codes) that no element reads (w = d*q). */
 typedef enum {
     QMM_Q8_0 = 0,
     QMM_Q4_0 = 1,
@@ -67,7 +72,10 @@ typedef enum {
     QMM_IQ4_NL = 8,
     QMM_IQ4_XS = 9,
     QMM_MXFP4 = 10,
-    QMM_NKINDS = 11
+    QMM_Q4_1 = 11,
+    QMM_Q5_1 = 12,
+    QMM_Q8_1 = 13,
+    QMM_NKINDS = 14
 } qmm_kind;
 
 /* Activation element type. f32 activations must be 4-byte aligned, f16

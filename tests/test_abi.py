@@ -25,15 +25,19 @@ def test_exports_every_declared_symbol(L):
 def test_kind_table(L):
     want = {"Q8_0": (34, 32), "Q4_0": (18, 32), "Q5_0": (22, 32), "Q4_K": (144, 256),
             "Q5_K": (176, 256), "Q6_K": (210, 256), "Q2_K": (84, 256), "Q3_K": (110, 256),
-            "IQ4_NL": (18, 32), "IQ4_XS": (136, 256), "MXFP4": (17, 32)}
+            "IQ4_NL": (18, 32), "IQ4_XS": (136, 256), "MXFP4": (17, 32),
+            "Q4_1": (20, 32), "Q5_1": (24, 32), "Q8_1": (36, 32)}
+    assert set(want) == set(qmm.KINDS)
     for k, g in want.items():
         assert qmm.kind_info(k) == g
         assert L.qmm_kind_name(qmm.KIND_ID[k]).decode() == k
         assert qmm.row_bytes(k, 4096) == 4096 // g[1] * g[0]
         assert qmm.row_bytes(k, g[1] + 16) == 0       # not a whole number of blocks
-    assert L.qmm_kind_name(11) is None and L.qmm_kind_name(-1) is None
-    # absent formats are not silently mapped (ferrox-cuda mul_mm.rs kind_by_name)
-    assert L.qmm_row_bytes(11, 256) == 0
+    assert L.qmm_kind_name(14) is None and L.qmm_kind_name(-1) is None
+    # absent formats are not silently mapped (ferrox-cuda mul_mm.rs kind_by_name):
+    # the grid-codebook kinds have no id at all
+    assert L.qmm_row_bytes(14, 256) == 0
+    assert not {"IQ1_S", "IQ2_XXS", "IQ3_S"} & set(qmm.KINDS)
     bb, be = ctypes.c_size_t(), ctypes.c_size_t()
     assert L.qmm_kind_info(42, ctypes.byref(bb), ctypes.byref(be)) == qmm.STATUS_ID["QMM_ERR_BAD_KIND"]
 
@@ -53,7 +57,7 @@ def _gemm(L, kind=1, W=FAKE, wb=1 << 30, X=FAKE, xdt=0, xe=1 << 30, Y=FAKE, ye=1
 
 
 @pytest.mark.parametrize("args,status", [
-    (dict(kind=11), "QMM_ERR_BAD_KIND"),
+    (dict(kind=14), "QMM_ERR_BAD_KIND"),
     (dict(kind=-1), "QMM_ERR_BAD_KIND"),
     (dict(M=0), "QMM_ERR_EMPTY_SHAPE"),
     (dict(N=0), "QMM_ERR_EMPTY_SHAPE"),
@@ -158,7 +162,7 @@ def test_moe_layer_refusals(L):
         return L.qmoe_ffn(a["kind"], a["gu"], a["gub"], a["gus"], a["dn"], a["dnb"], a["dns"], a["ne"], a["x"],
                           a["xe"], a["T"], a["dm"], a["dff"], a["ids"], a["w"], a["k"], a["y"], a["ye"], a["ws"],
                           a["wsb"], None)
-    assert m(kind=11) == S["QMM_ERR_BAD_KIND"]
+    assert m(kind=14) == S["QMM_ERR_BAD_KIND"]
     assert m(T=0) == S["QMM_ERR_EMPTY_SHAPE"]
     assert m(k=-1) == S["QMM_ERR_BAD_ARGUMENT"]
     assert m(ids=0) == S["QMM_ERR_NULL_POINTER"]

@@ -214,7 +214,8 @@ def oracle_full_product(orc, kind, w, M, K, x):
 
 
 @pytest.mark.parametrize("cfg,kind", [(synth.KQUANT, k) for k in synth.KQUANT["kinds"]] +
-                         [(synth.CODEBOOK, k) for k in synth.CODEBOOK["kinds"]])
+                         [(synth.CODEBOOK, k) for k in synth.CODEBOOK["kinds"]] +
+                         [(synth.LEGACY1, k) for k in synth.LEGACY1["kinds"]])
 def test_prefill_gemm_workload(Q, orc, cfg, kind):
     """The prefill workloads as configured, in the launch configuration the
     bench times: every output against the oracle's dequant + fp64 matmul, and
@@ -249,7 +250,8 @@ SCHEDULES = {"many_partials": (300, 8192, 150), "whole_inside": (24300, 2048, 12
 @pytest.mark.parametrize("case,kind", [("many_partials", "Q4_K"), ("many_partials", "IQ4_NL"),
                                        ("many_partials", "Q6_K"), ("whole_inside", "Q4_K"),
                                        ("whole_inside", "MXFP4"), ("one_per_cta", "Q5_K"),
-                                       ("one_per_cta", "IQ4_NL")])
+                                       ("one_per_cta", "IQ4_NL"), ("many_partials", "Q5_1"),
+                                       ("whole_inside", "Q4_1"), ("one_per_cta", "Q8_1")])
 def test_gemm_tile_schedules(Q, orc, case, kind):
     M, K, N = SCHEDULES[case]
     seed = sum(map(ord, case + kind))
@@ -453,6 +455,12 @@ def zero_valued_block(kind: str) -> np.ndarray:
     elif kind == "MXFP4":
         b[0] = 127
         b[1:17] = np.tile(np.array([0x00, 0x08, 0x80, 0x88], dtype=np.uint8), 4)  # +0 and -0
+    elif kind in ("Q4_1", "Q5_1"):
+        b[0:2] = d                                   # codes 0, min 0 (a nonzero min with
+                                                     # nonzero codes cancels only to rounding)
+    elif kind == "Q8_1":
+        b[0:2] = d
+        b[2:4] = d                                   # the unread field, nonzero; codes 0
     else:
         raise ValueError(kind)
     return b
@@ -548,7 +556,8 @@ def test_grouped_edge_cases(Q, orc, case):
 # fp32 activations on the tensor-core path, 16-bit outputs
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("cfg,kind", [(synth.KQUANT, "Q4_K"), (synth.KQUANT, "Q6_K"), (synth.KQUANT, "Q2_K"),
-                                      (synth.CODEBOOK, "IQ4_NL"), (synth.CODEBOOK, "MXFP4")])
+                                      (synth.CODEBOOK, "IQ4_NL"), (synth.CODEBOOK, "MXFP4"),
+                                      (synth.LEGACY1, "Q5_1")])
 def test_prefill_gemm_fp32_activations(Q, orc, cfg, kind):
     """fp32 activations at the workload shapes run on the tensor cores as
     (hi, lo) f16 pairs; every output against the oracle."""
@@ -563,7 +572,7 @@ def test_prefill_gemm_fp32_activations(Q, orc, cfg, kind):
     assert_within(Y.cpu().numpy(), y, tol, f"{kind} fp32 X, all {N * M} outputs")
 
 
-@pytest.mark.parametrize("kind", ["Q4_K", "Q5_K", "IQ4_XS", "Q8_0"])
+@pytest.mark.parametrize("kind", ["Q4_K", "Q5_K", "IQ4_XS", "Q8_0", "Q4_1", "Q5_1"])
 def test_fp32_activations_of_any_magnitude(Q, orc, kind):
     """Token rows far outside f16's range (1e30, 1e-30, mixed): the per-row
     power-of-two scale keeps the (hi, lo) split exact to about 2^-22."""
