@@ -1435,7 +1435,10 @@ Plan plan(const Problem& p) {
         // up to four columns per problem: measured on the 64-token MoE
         // projections, the 8-column decode (register-bound) lost more than
         // re-streaming the rows of the experts with over four tokens
-        const int want = pow2ceil(static_cast<int>((4 * p.N + p.n_experts - 1) / p.n_experts));
+        // (a split-K view has the same few columns in every slice: no more)
+        const int want = p.cols_per_expert > 0
+                             ? pow2ceil(p.cols_per_expert)
+                             : pow2ceil(static_cast<int>((4 * p.N + p.n_experts - 1) / p.n_experts));
         pl.ncmax = want < 4 ? want : 4;
         // item counts are int32 on the device
         if ((p.N + p.n_experts) * ((p.M + kRows - 1) / kRows) >= (int64_t(1) << 31)) return pl;

@@ -170,6 +170,7 @@ int launch_gemv_split(const Problem& p, int split, cudaStream_t s) {
     q.expert_stride = slice_bytes;
     q.n_experts = split;
     q.n_x_rows = A;
+    q.cols_per_expert = static_cast<int>(p.N);
     q.y_dtype = 0;
     const size_t part_bytes = up256(static_cast<size_t>(A) * p.M * 4);
     const size_t idx_bytes = up256(static_cast<size_t>(A) * 4);

@@ -55,6 +55,9 @@ struct Problem {
     // X[row * x_stride + K + k]
     int x_mode = 0;
     int64_t x_stride = 0;
+    // grouped: every expert has exactly this many assignments (a split-K view),
+    // or 0 (unknown, routed tokens)
+    int cols_per_expert = 0;
     unsigned* err = nullptr; // device latch
 };
 
