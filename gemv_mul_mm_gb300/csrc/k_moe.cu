@@ -36,8 +36,11 @@ __global__ void k_moe_rows(int32_t* __restrict__ row_gu, int32_t* __restrict__ r
 }
 
 // Y[t * M + m] = sum_j w[t * top_k + j] * O[(t * top_k + j) * M + m]
+// Launched as a programmatic dependent of the down projection: it may be
+// resident before that grid ends, and reads O only after the wait.
 __global__ void k_moe_combine(const float* __restrict__ O, const float* __restrict__ w, float* __restrict__ Y,
                               int64_t T, int top_k, int64_t M) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t total = T * M;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -127,9 +130,19 @@ int launch_moe_ffn(int kind, const uint8_t* W_gu, size_t gu_stride, size_t gu_ro
     if (launch_gemv_stream(pd, s) != cudaSuccess) return QMM_ERR_CUDA;
     const int64_t total = T * d_model;
     const int b2 = static_cast<int>(imin64((total + threads - 1) / threads, 4096));
-    k_moe_combine<<<b2, threads, 0, s>>>(sc.dn, w, Y, T, top_k, d_model);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(b2));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_moe_combine, static_cast<const float*>(sc.dn), w, Y, T, top_k,
+                                             d_model);
     count_launch(1);
-    return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
 }  // namespace qmm

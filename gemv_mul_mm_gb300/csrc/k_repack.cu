@@ -59,8 +59,10 @@ __global__ void k_split_rows(int32_t* __restrict__ x_row, int32_t* __restrict__ 
 }
 
 // Y[n * M + m] = sum_e part[(n * split + e) * M + m], in slice order.
+// A programmatic dependent of the GEMV: reads the partials after the wait.
 __global__ void k_split_reduce(const float* __restrict__ part, float* __restrict__ Y, int y_dtype, int64_t N,
                                int64_t M, int split) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t total = N * M;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -191,10 +193,19 @@ int launch_gemv_split(const Problem& p, int split, cudaStream_t s) {
     if (cudaGetLastError() != cudaSuccess) return QMM_ERR_CUDA;
     if (launch_gemv_stream(q, s) != cudaSuccess) return QMM_ERR_CUDA;
     const int64_t total = p.N * p.M;
-    k_split_reduce<<<static_cast<int>(imin64((total + threads - 1) / threads, 4096)), threads, 0, s>>>(
-        part, p.Y, p.y_dtype, p.N, p.M, split);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(imin64((total + threads - 1) / threads, 4096)));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_split_reduce, static_cast<const float*>(part), p.Y, p.y_dtype,
+                                             p.N, p.M, split);
     count_launch(1);
-    return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
 }  // namespace qmm
