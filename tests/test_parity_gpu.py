@@ -618,3 +618,44 @@ def test_sixteen_bit_outputs(Q, orc, out, kind, N, path):
     half_ulp = np.abs(y) * (2.0 ** -11 if out == "f16" else 2.0 ** -8)
     bad = ~(np.abs(got - y) <= tol + half_ulp)
     assert not bad.any(), f"{int(bad.sum())} outputs outside the bar"
+
+
+# ---------------------------------------------------------------------------
+# the tensor-core GEMM's f16 operand fold at its worst case
+# ---------------------------------------------------------------------------
+def fold_worst_block(kind):
+    """A block whose every element's code times sub-scale is an odd integer just
+    above 2048, where f16 rounds by half a spacing of 2 (relative 4.8e-4), all
+    with the same sign: Q6_K sc = 77, q - 32 = 27 (2079); IQ4_XS ls - 32 = -25,
+    KV = -83 (2075). d has 11 significant bits."""
+    bb, _ = synth.block_geometry(kind)
+    b = np.zeros(bb, dtype=np.uint8)
+    d = (0x1BFF).to_bytes(2, "little")
+    if kind == "Q6_K":
+        b[0:128] = 0xBB                  # low nibbles 11 (q = 59 = 11 + 16 * 3)
+        b[128:192] = 0xFF                # high 2-bit fields 3
+        b[192:208] = 77                  # int8 sub-scales
+        b[208:210] = list(d)
+    else:
+        b[0:2] = list(d)
+        b[2:4] = 0x00                    # scales_h: high bits 0
+        b[4:8] = 0x77                    # scales_l: ls = 7 -> ls - 32 = -25
+        b[8:136] = 0x22                  # codes 2 -> KV = -83
+    return b
+
+
+@pytest.mark.parametrize("kind", ["Q6_K", "IQ4_XS"])
+def test_operand_fold_worst_case(Q, orc, kind):
+    """Every weight of a long row rounds the same way when its integer operand
+    is folded into f16, and every activation is positive, so the rounding adds
+    up coherently over K = 16384: the product stays within the bar."""
+    M, K, N = 128, 16384, 33
+    w = np.tile(fold_worst_block(kind), M * (K // 256))
+    x = (0.5 + 0.5 * synth.Stream(91).uniform(N * K)).astype(np.float16).reshape(N, K)
+    deq = orc.dequant(kind, w, 1, K)[0]
+    assert np.all(deq == deq[0]) and deq[0] != 0, "one value everywhere"
+    y, tol = orc.gemm(kind, w, M, K, x, N)
+    Y = sentinel((N, M))
+    Q.qgemm(kind, dev(w), dev(x), M, K, N, Y=Y)
+    assert Q.last_path() == Q.PATH_TC
+    assert_within(Y.cpu().numpy(), y, tol, f"{kind} operand fold, worst case")
