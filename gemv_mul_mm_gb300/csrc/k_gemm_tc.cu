@@ -1240,7 +1240,7 @@ TcKernel tc_kernel(int* smem_bytes) {
 }
 
 // Per-group activation sums for the min term: out[n][s][0..G) = hi, [G..2G) = lo
-// with hi = f16(sum), lo = f16(sum - hi); groups of 32 (Q4_K, Q5_K) or 16 (Q2_K).
+// with hi = f16(sum), lo = f16(sum - hi); groups of 32 (Q4_K, Q5_K, Q4_1, Q5_1) or 16 (Q2_K).
 // One thread per group, reading its 16 or 32 halves with 16-byte loads (the
 // rows of X are 16-byte aligned and K is a multiple of 256).
 __global__ void k_xsums(const __half* __restrict__ X, int N, int K, int gsize, int G, __half* __restrict__ out) {

@@ -409,7 +409,7 @@ __device__ __forceinline__ void unit_q8_0(const uint8_t* u, const float* xs, int
 // exponent of 2^23 (one byte permute) reads 2^23 + c_k, and one packed
 // subtract of 2^23 + bias leaves c_k - bias exactly. Packed FMAs then add
 // (c_k - bias) * x_k into per-group partial sums, which the group's fp32 scale
-// multiplies afterwards (the minimum term of Q4_K / Q5_K / Q2_K multiplies
+// multiplies afterwards (the minimum term of Q4_K / Q5_K / Q2_K / Q4_1 / Q5_1 multiplies
 // the group's activation sum). Codebooks are looked up four nibbles at a time
 // in registers (byte permutes, see lut16), never in memory.
 // ---------------------------------------------------------------------------

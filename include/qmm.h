@@ -162,9 +162,9 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
  * its largest magnitude in [2^9, 2^10) and splits it into hi = f16(x) and
  * lo = f16(x - hi) (together exact to about 2^-22 relative); the epilogue adds
  * the two products and removes the scale. This doubles the tensor-core work of
- * the call against f16 activations. With f16 activations, Q4_K, Q5_K and Q2_K
- * carry the sums of each 32 (Q2_K: 16) consecutive activations in f16: their
- * magnitudes must stay below 65504.
+ * the call against f16 activations. With f16 activations, Q4_K, Q5_K, Q2_K,
+ * Q4_1 and Q5_1 carry the sums of each 32 (Q2_K: 16) consecutive activations
+ * in f16: their magnitudes must stay below 65504.
  *
  *   W, w_bytes   as qgemv
  *   X            device, N * K activations of x_dtype, row-major; x_elems its size
@@ -174,9 +174,9 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
  *
  * Workspace: the tensor-core path keeps its scratch in a per-device workspace
  * the library owns and grows on demand (cudaMalloc): the f16 (hi, lo) rows of
- * fp32 activations and their scales (4 * N * K + 4 * N bytes), for Q4_K, Q5_K
- * and Q2_K the per-group activation sums (N * K/16 f16 values at most, twice
- * that for fp32 activations), and, when the
+ * fp32 activations and their scales (4 * N * K + 4 * N bytes), for Q4_K,
+ * Q5_K, Q2_K, Q4_1 and Q5_1 the per-group activation sums (N * K/16 f16
+ * values at most, twice that for fp32 activations), and, when the
  * 128 x 128 output tiles do not fill the GPU evenly, the partial tiles of
  * the tiles whose K range several CTAs share (2 * 64 KiB per SM). Those
  * partial sums are added in a fixed order by a second kernel, so results are
@@ -227,13 +227,13 @@ QMM_API int qgemm_ex(int kind, const void* W, size_t w_bytes, const void* X, int
  * of the sums can differ from qgemm's), but only on the tensor-core path:
  * f16 activations, K a multiple of 256, 16-byte aligned W and X, rows a
  * multiple of 16 bytes (QMM_ERR_UNIMPLEMENTED otherwise). The per-group
- * activation sums that Q4_K, Q5_K and Q2_K need go to a fixed 4 MiB device
- * array compiled into the library (held on every GPU that loads it, until
- * the process exits) instead of a grown workspace; a problem whose sums need
- * more, N * (K / 256) * 32 bytes for Q4_K / Q5_K or N * (K / 256) * 64 bytes
- * for Q2_K above 4 MiB, returns QMM_ERR_NOALLOC_LIMIT before anything is
- * launched. Each call rewrites all the scratch it reads, so nothing is left
- * to clear between calls. The array is shared by every call: calls that can
+ * activation sums that Q4_K, Q5_K, Q2_K, Q4_1 and Q5_1 need go to a fixed
+ * 4 MiB device array compiled into the library (held on every GPU that loads
+ * it, until the process exits) instead of a grown workspace; a problem whose
+ * sums need more, N * (K / 256) * 32 bytes for Q4_K / Q5_K / Q4_1 / Q5_1 or
+ * N * (K / 256) * 64 bytes for Q2_K above 4 MiB, returns QMM_ERR_NOALLOC_LIMIT
+ * before anything is launched. Each call rewrites all the scratch it reads,
+ * so nothing is left to clear between calls. The array is shared by every call: calls that can
  * overlap on the GPU (different streams, same device) race on it and must
  * be ordered by the caller. The first call on a device looks the array's
  * address up with cudaGetSymbolAddress (no allocation), once per device.
