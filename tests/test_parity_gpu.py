@@ -157,6 +157,8 @@ def test_tiny_q4_0_qgemm(Q, orc):
 
 @pytest.mark.parametrize("kind", ["Q8_0", "Q4_0"])
 def test_decode_gemv_full(Q, orc, kind):
+    """The decode workload as configured: every output against the oracle's
+    own element-indexed product."""
     c = synth.DECODE
     M, K = c["M"], c["K"]
     w = synth.workload_weights(c, kind)
@@ -166,6 +168,22 @@ def test_decode_gemv_full(Q, orc, kind):
     Q.qgemv(kind, dev(w), dev(x), M, K, y=Y.view(-1))
     assert Q.last_path() == Q.PATH_GEMV
     assert_within(Y.cpu().numpy(), y, tol, f"decode {kind}")
+
+
+@pytest.mark.parametrize("kind", [k for k in KINDS if k not in ("Q8_0", "Q4_0")])
+def test_decode_shape_gemv_every_kind(Q, orc, kind):
+    """Every other kind at the decode shape (M 14336, K 4096, one fp32
+    column, the per-kind table of the bench): all outputs against the oracle's
+    dequant + fp64 product."""
+    c = synth.DECODE
+    M, K = c["M"], c["K"]
+    w = synth.quant_weights(kind, M, K, synth.config_seed(1, kind))
+    x = synth.workload_x(c, "Q4_0")
+    y, tol = oracle_full_product(orc, kind, w, M, K, x)
+    Y = sentinel((1, M))
+    Q.qgemv(kind, dev(w), dev(x), M, K, y=Y.view(-1), weights_const=True)
+    assert Q.last_path() == Q.PATH_GEMV
+    assert_within(Y.cpu().numpy(), y, tol, f"decode shape {kind}")
 
 
 @pytest.mark.parametrize("kind", ["Q4_0", "Q8_0", "IQ4_NL"])

@@ -35,7 +35,8 @@ def test_repack_bytes_match_the_layout(Q, kind):
 @pytest.mark.parametrize("M,K,N,split,xdt", [(130, 1024, 1, 0, "f32"), (130, 1024, 3, 2, "f32"),
                                              (2048, 4096, 1, 0, "f32"), (2048, 4096, 8, 4, "f16"),
                                              (256, 4096, 1, 16, "f32"), (1000, 2048, 2, 1, "f32"),
-                                             (14336, 4096, 1, 0, "f32")])
+                                             (14336, 4096, 1, 0, "f32"), (2048, 14336, 1, 0, "f32"),
+                                             (2048, 14336, 5, 0, "f32")])
 def test_repacked_gemv_matches_oracle(Q, orc, kind, M, K, N, split, xdt):
     w = synth.quant_weights(kind, M, K, 51 + M + N)
     x = synth.activations(N, K, 52 + N, xdt)
