@@ -39,7 +39,7 @@ def _noalloc(Q, kind, W, X, Y, M, K, N):
                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-@pytest.mark.parametrize("kind", ["Q4_K", "Q2_K", "Q5_K", "IQ4_NL"])
+@pytest.mark.parametrize("kind", ["Q4_K", "Q2_K", "Q5_K", "IQ4_NL", "Q4_1"])
 def test_noalloc_matches_oracle_and_qgemm_on_two_calls_in_a_row(Q, orc, kind):
     import torch
     problems = [(384, 2048, 160, 11), (256, 4096, 96, 12)]   # (M, K, N, seed)
