@@ -904,7 +904,8 @@ template <int KIND> struct PipeSB {
     static constexpr int D2COL = D1COL + 2 * BN;              // 384 (formats with mins)
     static constexpr int MINB = Mins<KIND>::TILES * MIN_TILE;
     static constexpr int RAWB = BM * Raw<KIND>::BOXB;
-    static constexpr int FIXED = NS * X_HALF + 2 * MINB + 2 * BM * 8 * 4 + 2048;
+    static constexpr int SCD = 4;                             // scale buffers (super-steps in flight)
+    static constexpr int FIXED = NS * X_HALF + 2 * MINB + SCD * BM * 2 * 4 + 2048;
     static constexpr int FREE = 226 * 1024 - FIXED;
     static constexpr int RS = FREE >= 4 * RAWB ? 4 : FREE >= 3 * RAWB ? 3 : 2;
     static_assert(FIXED + RS * RAWB <= 226 * 1024, "shared memory");
@@ -918,10 +919,10 @@ struct LayoutSB {
     static constexpr int OFF_RAW = OFF_X + P::NS * X_HALF;
     static constexpr int OFF_AMIN = (OFF_RAW + P::RS * P::RAWB + 1023) & ~1023;
     static constexpr int OFF_BMIN = OFF_AMIN + P::MINB;
-    static constexpr int OFF_SC = OFF_BMIN + P::MINB;                    // [2][128][8] floats
-    static constexpr int OFF_BAR = OFF_SC + 2 * BM * 8 * 4;
-    // raw_full/empty[RS], a_full[NS], x_full[NS], done[NS], d_empty, sc_full/empty[2], fin
-    static constexpr int NBAR = 2 * P::RS + 3 * P::NS + 1 + 4 + 1;
+    static constexpr int OFF_SC = OFF_BMIN + P::MINB;                    // [SCD][128][2] floats
+    static constexpr int OFF_BAR = OFF_SC + P::SCD * BM * 2 * 4;
+    // raw_full/empty[RS], a_full[NS], x_full[NS], done[NS], d_empty[2], sc_full/empty[SCD], fin
+    static constexpr int NBAR = 2 * P::RS + 3 * P::NS + 2 + 2 * P::SCD + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16 + 1024;                   // + alignment slack
 };
@@ -935,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using P = PipeSB<KIND>;
     using L = LayoutSB<KIND>;
     static_assert(!TcGeo<KIND>::PER32, "super-block formats only");
-    constexpr int NS = P::NS, RS = P::RS;
+    constexpr int NS = P::NS, RS = P::RS, SCD = P::SCD;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -950,10 +951,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* a_full = raw_empty + RS;
     uint64_t* x_full = a_full + NS;
     uint64_t* done = x_full + NS;
-    uint64_t* d_empty = done + NS;
-    uint64_t* sc_full = d_empty + 1;
-    uint64_t* sc_empty = sc_full + 2;
-    uint64_t* fin = sc_empty + 2;
+    uint64_t* d_empty = done + NS;   // [2]: the epilogue is done with super-step s (index s & 1)
+    uint64_t* sc_full = d_empty + 2;
+    uint64_t* sc_empty = sc_full + SCD;
+    uint64_t* fin = sc_empty + SCD;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);
 
@@ -970,8 +971,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&x_full[i], 1);
             mbar_init(&done[i], 1);
         }
-        mbar_init(d_empty, kNumEpi);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 2; ++i) mbar_init(&d_empty[i], kNumEpi);
+        for (int i = 0; i < SCD; ++i) {
             mbar_init(&sc_full[i], kNumDec);
             mbar_init(&sc_empty[i], kNumEpi);
         }
@@ -1085,9 +1086,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int i = h % NS, u = h / NS, s = h >> 1;
                 ok = spin_bar(&a_full[i], u & 1, abort_flag, a.err);
                 if (ok) ok = spin_bar(&x_full[i], u & 1, abort_flag, a.err);
-                // the second half of super-step s rewrites the min term and
-                // completes D1[s & 1]: the epilogue must be done with s - 1
-                if (ok && (h & 1) && s >= 1) ok = spin_bar(d_empty, (s - 1) & 1, abort_flag, a.err);
+                if constexpr (MN::ON) {
+                    // the second half of super-step s rewrites the (single) min
+                    // term: the epilogue must be done with s - 1
+                    if (ok && (h & 1) && s >= 1)
+                        ok = spin_bar(&d_empty[(s - 1) & 1], ((s - 1) >> 1) & 1, abort_flag, a.err);
+                } else {
+                    // super-step s overwrites D1[s & 1]: the epilogue must be
+                    // done with s - 2 (one super-step of slack for the epilogue)
+                    if (ok && !(h & 1) && s >= 2)
+                        ok = spin_bar(&d_empty[s & 1], ((s - 2) >> 1) & 1, abort_flag, a.err);
+                }
             }
             bar_red_and(kBarHand + (h & 1), 64, lane != 0 || ok);
         }
@@ -1102,15 +1111,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rs = s % RS;
             bool ok = warp_wait_bar(&raw_full[rs], (s / RS) & 1, abort_flag, a.err);
             const uint8_t* row = raw + rs * R::STAGE + r * R::BOXB + ((ks * R::SBB) & 15);
-            if (ok && s >= 2) ok = warp_wait_bar(&sc_empty[s & 1], ((s >> 1) - 1) & 1, abort_flag, a.err);
+            if (ok && s >= SCD) ok = warp_wait_bar(&sc_empty[s % SCD], ((s / SCD) - 1) & 1, abort_flag, a.err);
             if (ok) {
                 const float2 dd = scale256<KIND>(row);
-                float* sc = sbuf + ((s & 1) * BM + r) * 8;
+                float* sc = sbuf + ((s % SCD) * BM + r) * 2;
                 sc[0] = dd.x;
                 sc[1] = dd.y;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sc_full[s & 1]);
+            if (lane == 0) mbar_arrive(&sc_full[s % SCD]);
             uint32_t scw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
             if (ok) FastDec<KIND>::pre(row, scw);
 #pragma unroll 1
@@ -1172,8 +1181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int seg_end = min(nloc, s + a.nsup - es);
             const bool whole = es == 0 && seg_end - s == a.nsup;
             for (; s < seg_end; ++s) {
-                const float* sc = sbuf + ((s & 1) * BM + r) * 8;
-                warp_wait_bar(&sc_full[s & 1], (s >> 1) & 1, abort_flag, a.err);
+                const float* sc = sbuf + ((s % SCD) * BM + r) * 2;
+                warp_wait_bar(&sc_full[s % SCD], (s / SCD) & 1, abort_flag, a.err);
                 const int h = 2 * s + 1;
                 const bool ok = warp_wait_bar(&done[h % NS], (h / NS) & 1, abort_flag, a.err);
                 tc_fence_after();
@@ -1204,8 +1213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(d_empty);
-                    mbar_arrive(&sc_empty[s & 1]);
+                    mbar_arrive(&d_empty[s & 1]);
+                    mbar_arrive(&sc_empty[s % SCD]);
                 }
             }
             if (!*abort_flag) store_tile(a, span, et, whole, half, r, acc);
