@@ -298,7 +298,7 @@ __device__ __forceinline__ float codebook_entry(int c) {
 //   Q4_0    q - 8                                    d        per 32
 //   Q5_0    q - 16                                   d        per 32
 //   IQ4_NL  KV[c]                                    d        per 32
-//   MXFP4   E2M1[c]                                  2^(e-127) per 32
+//   MXFP4   E2M1[c] * 2^(e - e_max)  (exact unless e_max - e > 24)   2^(e_max-127) per 256
 //   Q8_1    q                                        d        per 32
 //   Q4_1    q                                        d        per 32;   mins: m (an f16)
 //   Q5_1    q                                        d        per 32;   mins: m (an f16)
@@ -310,7 +310,9 @@ __device__ __forceinline__ float codebook_entry(int c) {
 //   IQ4_XS  (ls - 32) * KV[c]   (<= 4064; rounds once above 2048)   d per 256
 // ---------------------------------------------------------------------------
 template <int KIND> struct TcGeo {
-    static constexpr bool PER32 = Geo<KIND>::BE == 32;                       // scale per 32-element block
+    // scale per 32-element block (MXFP4 folds its block exponents into the
+    // operands and keeps one power of two per 256 elements instead)
+    static constexpr bool PER32 = Geo<KIND>::BE == 32 && KIND != MXFP4;
     static constexpr bool MINS = KIND == Q4_K || KIND == Q5_K || KIND == Q2_K || KIND == Q4_1 || KIND == Q5_1;
     static constexpr int MIN_GROUPS = KIND == Q2_K ? 16 : 8;                 // min groups per 256
 };
@@ -332,7 +334,13 @@ __device__ __forceinline__ float2 scale256(const uint8_t* b) {
     else if constexpr (KIND == Q6_K) return make_float2(h2f(ld16(b, 208)), 0.f);
     else if constexpr (KIND == Q2_K) return make_float2(h2f(ld16(b, 80)), h2f(ld16(b, 82)));
     else if constexpr (KIND == Q3_K) return make_float2(h2f(ld16(b, 108)), 0.f);
-    else return make_float2(h2f(ld16(b, 0)), 0.f);  // IQ4_XS
+    else if constexpr (KIND == MXFP4) {
+        // the largest of the eight block exponents: 2^(e_max - 127)
+        uint32_t e = 0;
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk) e = max(e, static_cast<uint32_t>(b[17 * blk]));
+        return make_float2(e8m0f(e), 0.f);
+    } else return make_float2(h2f(ld16(b, 0)), 0.f);  // IQ4_XS
 }
 
 // Runtime kind -> template dispatch helper for the streaming GEMV, which also

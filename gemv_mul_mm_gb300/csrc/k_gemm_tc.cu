@@ -19,8 +19,9 @@
 //     accumulators, one fresh accumulator per promotion unit;
 //   * warps 6-13 read each finished unit from TMEM (tcgen05.ld) and apply the
 //     fp32 scales to the PARTIAL SUMS: acc += d * D1 - dmin * D2 per 256-element
-//     super-block (K-quants, IQ4_XS) or acc += d * D per 32-element block
-//     (Q8_0, Q4_0, Q5_0, IQ4_NL, MXFP4), then store Y.
+//     super-block (K-quants, IQ4_XS, and MXFP4 with its block exponents folded
+//     into the operands) or acc += d * D per 32-element block (Q8_0, Q4_0,
+//     Q5_0, IQ4_NL, Q4_1, Q5_1, Q8_1), then store Y.
 // Keeping A in TMEM halves the shared-memory traffic per MMA (only B is read
 // from shared memory) and spares the decoders the swizzled stores.
 // The K-quant mins (-dmin * sum_s m_s * sum_{k in s} x_k) come out of a second,
@@ -873,8 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // The formats with one fp32 scale per 256-element super-block (Q4_K, Q5_K,
-// Q6_K, Q2_K, Q3_K, IQ4_XS) run a leaner pipeline, k_gemm_sb. Its unit is a
-// half-step: two sub-steps (K = 128, eight MMAs). Each half-step's MMAs end
+// Q6_K, Q2_K, Q3_K, IQ4_XS, and MXFP4 through its exponent fold) run a leaner
+// pipeline, k_gemm_sb. Its unit is a half-step: two sub-steps (K = 128, eight
+// MMAs). Each half-step's MMAs end
 // with ONE tcgen05.commit on the stage's `done` barrier, which releases at
 // once everything the half-step read -- its A stage in tensor memory, its
 // activation stage (and, on the second half of a super-step, the min-term

@@ -151,8 +151,8 @@ __device__ __forceinline__ void ld_words(const uint8_t* p, uint32_t (&w)[NW]) {
 template <int KIND> struct FastDec;
 // Formats whose decoder takes per-super-block scale words (pre / sub_pre).
 template <int KIND> struct FastDecPre {
-    static constexpr bool ON =
-        KIND == Q4_K || KIND == Q5_K || KIND == Q6_K || KIND == Q2_K || KIND == Q3_K || KIND == IQ4_XS;
+    static constexpr bool ON = KIND == Q4_K || KIND == Q5_K || KIND == Q6_K || KIND == Q2_K || KIND == Q3_K ||
+                               KIND == IQ4_XS || KIND == MXFP4;
 };
 
 // ---------------------------------------------------------------------------
@@ -312,14 +312,40 @@ template <> struct FastDec<IQ4_NL> {
     }
 };
 
+// MXFP4 on the super-block pipeline: the eight block exponents of a
+// 256-element super-step are folded into the operands relative to the largest
+// one, e_max (2^(e_max - 127) multiplies the super-block's partial sums): a
+// block's codes are scaled by 2^-(e_max - e), an exact f16 power of two (zero
+// below 2^-24, when the exponents of one super-step span more than 24).
+__device__ __forceinline__ uint32_t h2pow2neg(uint32_t k) {
+    const uint32_t h = k <= 14u ? ((15u - k) << 10) : (k <= 24u ? (1u << (24u - k)) : 0u);
+    return h | (h << 16);
+}
 template <> struct FastDec<MXFP4> {
-    __device__ __forceinline__ static void sub(const uint8_t* row, int q, uint32_t (&o)[32]) {
+    // scw[b] = 2^-(e_max - e_b) for the super-step's eight blocks, f16x2
+    __device__ __forceinline__ static void pre(const uint8_t* row, uint32_t (&scw)[8]) {
+        uint32_t e[8], emax = 0;
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk) {
+            e[blk] = row[17 * blk];
+            emax = max(emax, e[blk]);
+        }
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk) scw[blk] = h2pow2neg(emax - e[blk]);
+    }
+    __device__ __forceinline__ static void sub_pre(const uint8_t* row, int q, uint32_t (&o)[32],
+                                                   const uint32_t (&scw)[8]) {
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
+            const int j = 2 * q + hb;
+            const uint32_t sc = q == 0 ? (hb ? scw[1] : scw[0])
+                              : q == 1 ? (hb ? scw[3] : scw[2])
+                              : q == 2 ? (hb ? scw[5] : scw[4])
+                                       : (hb ? scw[7] : scw[6]);
             uint32_t w[4];
-            ld_words<4, 1>(row + (2 * q + hb) * 17 + 1, w);
-            // 512 + b / 2 - 576 = E2M1 value
-            lut_block<E2m1Table, kMagB512, h2int(-576)>(w, 0u, 0u, false, o + 16 * hb);
+            ld_words<4, 1>(row + 17 * j + 1, w);
+            // (512 + b / 2) * s - 576 * s = E2M1 value * s, one rounding
+            lut_block<E2m1Table, kMagB512, 0u>(w, sc, hmul2_u(sc, h2int(-576)), true, o + 16 * hb);
         }
     }
 };
