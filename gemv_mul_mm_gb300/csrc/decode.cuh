@@ -323,8 +323,8 @@ template <int KIND> struct TcGeo {
 // fp32 scale of a 32-element block (PER32 formats).
 template <int KIND>
 __device__ __forceinline__ float scale32(const uint8_t* b) {
-    if constexpr (KIND == MXFP4) return e8m0f(b[0]);
-    else return h2f(ld16(b, 0));
+    static_assert(TcGeo<KIND>::PER32, "per-32 formats: an f16 scale at byte 0");
+    return h2f(ld16(b, 0));
 }
 
 // Super-block d and dmin (PER32 == false).
