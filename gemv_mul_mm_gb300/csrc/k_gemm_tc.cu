@@ -900,6 +900,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // activation producer refill a stage only after its previous use completed;
 // the epilogue reads super-step s before the waiter lets the second half of
 // super-step s + 1 issue (that half waits for the epilogue's d_empty of s).
+// Half-step h's completion is signalled on done[h % 4] whatever the number of
+// stages: with two A stages and two decoder sets, a stage's previous user is
+// the other set, and a barrier per stage could then be two phases ahead of a
+// set's last wait on it; with four barriers, every waiter for half-step h has
+// itself seen h - 4 complete. Likewise, where the raw stages are odd in
+// number, a decoder first waits until the other set has released its stage
+// (raw_empty) before it waits for the stage's next load.
 // ---------------------------------------------------------------------------
 constexpr int kHalfSubs = 2;                   // sub-steps per half-step
 constexpr int kACols2 = kHalfSubs * kACols;    // 64 TMEM columns per A stage
@@ -913,6 +920,7 @@ template <int KIND> struct PipeSB {
     static constexpr int MINB = Mins<KIND>::TILES * MIN_TILE;
     static constexpr int RAWB = BM * Raw<KIND>::BOXB;
     static constexpr int SCD = 4;                             // scale buffers (super-steps in flight)
+    static constexpr int NDONE = 4;                           // completion barriers, done[h % 4]
     static constexpr int FIXED = NS * X_HALF + 2 * MINB + SCD * BM * 2 * 4 + 2048;
     static constexpr int FREE = 226 * 1024 - FIXED;
     static constexpr int RS = FREE >= 4 * RAWB ? 4 : FREE >= 3 * RAWB ? 3 : 2;
@@ -929,8 +937,8 @@ struct LayoutSB {
     static constexpr int OFF_BMIN = OFF_AMIN + P::MINB;
     static constexpr int OFF_SC = OFF_BMIN + P::MINB;                    // [SCD][128][2] floats
     static constexpr int OFF_BAR = OFF_SC + P::SCD * BM * 2 * 4;
-    // raw_full/empty[RS], a_full[NS], x_full[NS], done[NS], d_empty[2], sc_full/empty[SCD], fin
-    static constexpr int NBAR = 2 * P::RS + 3 * P::NS + 2 + 2 * P::SCD + 1;
+    // raw_full/empty[RS], a_full[NS], x_full[NS], done[NDONE], d_empty[2], sc_full/empty[SCD], fin
+    static constexpr int NBAR = 2 * P::RS + 2 * P::NS + P::NDONE + 2 + 2 * P::SCD + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16 + 1024;                   // + alignment slack
 };
@@ -944,7 +952,8 @@ __global__ void __launch_bounds__(SBThreads<KIND>::V, 1)
     using P = PipeSB<KIND>;
     using L = LayoutSB<KIND>;
     static_assert(!TcGeo<KIND>::PER32, "super-block formats only");
-    constexpr int NS = P::NS, RS = P::RS, SCD = P::SCD;
+    constexpr int NS = P::NS, RS = P::RS, SCD = P::SCD, NDONE = P::NDONE;
+    static_assert(NDONE == 4 && NDONE % NS == 0, "done[h % 4]: each barrier belongs to one stage");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -959,7 +968,7 @@ __global__ void __launch_bounds__(SBThreads<KIND>::V, 1)
     uint64_t* a_full = raw_empty + RS;
     uint64_t* x_full = a_full + NS;
     uint64_t* done = x_full + NS;
-    uint64_t* d_empty = done + NS;   // [2]: the epilogue is done with super-step s (index s & 1)
+    uint64_t* d_empty = done + NDONE;   // [2]: the epilogue is done with super-step s (index s & 1)
     uint64_t* sc_full = d_empty + 2;
     uint64_t* sc_empty = sc_full + SCD;
     uint64_t* fin = sc_empty + SCD;
@@ -977,8 +986,8 @@ __global__ void __launch_bounds__(SBThreads<KIND>::V, 1)
         for (int i = 0; i < NS; ++i) {
             mbar_init(&a_full[i], kNumDec);
             mbar_init(&x_full[i], 1);
-            mbar_init(&done[i], 1);
         }
+        for (int i = 0; i < NDONE; ++i) mbar_init(&done[i], 1);
         for (int i = 0; i < 2; ++i) mbar_init(&d_empty[i], kNumEpi);
         for (int i = 0; i < SCD; ++i) {
             mbar_init(&sc_full[i], kNumDec);
@@ -1026,7 +1035,7 @@ __global__ void __launch_bounds__(SBThreads<KIND>::V, 1)
             for (; h < nh; ++h) {
                 const int half = h & 1, i = h % NS;
                 if (h > 0 && half == 0) st.next(a);
-                if (h >= NS && !wait_bar(&done[i], ((h / NS) - 1) & 1, abort_flag, a.err)) break;
+                if (h >= NS && !wait_bar(&done[(h - NS) % NDONE], ((h - NS) / NDONE) & 1, abort_flag, a.err)) break;
                 const int k0 = st.s * KSUP + half * kHalfSubs * KSUB;
                 mbar_arrive_expect_tx(&x_full[i], X_HALF + ((MN::ON && half) ? P::MINB : 0));
                 tma2d(x_tiles + i * X_HALF, &tmX, k0, st.n0, &x_full[i]);
@@ -1076,7 +1085,7 @@ __global__ void __launch_bounds__(SBThreads<KIND>::V, 1)
                         for (int t = 0; t < MN::TILES; ++t) tc_mma(tmem + P::D2COL, adesc[t], bdesc[t], kIdesc, t);
                     }
                 }
-                tc_commit(&done[i]);
+                tc_commit(&done[h % NDONE]);
             }
             __syncwarp();
         }
@@ -1121,7 +1130,11 @@ __global__ void __launch_bounds__(SBThreads<KIND>::V, 1)
         for (int s = dset; s < nloc; s += dstep) {
             const int ks = static_cast<int>((static_cast<int64_t>(span.s0) + s) % a.nsup);   // super-step within the row
             const int rs = s % RS;
-            bool ok = warp_wait_bar(&raw_full[rs], (s / RS) & 1, abort_flag, a.err);
+            bool ok = true;
+            // the stage's previous load was decoded by the other set: its
+            // release bounds raw_full's phase (see above)
+            if (RS % dstep != 0 && s >= RS) ok = warp_wait_bar(&raw_empty[rs], ((s / RS) - 1) & 1, abort_flag, a.err);
+            if (ok) ok = warp_wait_bar(&raw_full[rs], (s / RS) & 1, abort_flag, a.err);
             const uint8_t* row = raw + rs * R::STAGE + r * R::BOXB + ((ks * R::SBB) & 15);
             if (ok && s >= SCD) ok = warp_wait_bar(&sc_empty[s % SCD], ((s / SCD) - 1) & 1, abort_flag, a.err);
             if (ok) {
@@ -1145,7 +1158,7 @@ __global__ void __launch_bounds__(SBThreads<KIND>::V, 1)
                 // decode first, then wait for the stage, so the decode stays off
                 // the stage's round trip (ok is warp-uniform: tcgen05.st is
                 // warp-collective)
-                if (ok && h >= NS) ok = warp_wait_bar<true>(&done[i], ((h / NS) - 1) & 1, abort_flag, a.err);
+                if (ok && h >= NS) ok = warp_wait_bar<true>(&done[(h - NS) % NDONE], ((h - NS) / NDONE) & 1, abort_flag, a.err);
                 if constexpr (MN::ON) {
                     if (half && ok) {
                         // A_min tile(s) of super-step s: 32B-swizzled K-major, 16 f16
@@ -1196,7 +1209,7 @@ __global__ void __launch_bounds__(SBThreads<KIND>::V, 1)
                 const float* sc = sbuf + ((s % SCD) * BM + r) * 2;
                 warp_wait_bar(&sc_full[s % SCD], (s / SCD) & 1, abort_flag, a.err);
                 const int h = 2 * s + 1;
-                const bool ok = warp_wait_bar(&done[h % NS], (h / NS) & 1, abort_flag, a.err);
+                const bool ok = warp_wait_bar(&done[h % NDONE], (h / NDONE) & 1, abort_flag, a.err);
                 tc_fence_after();
                 const float2 d2 = make_float2(sc[0], sc[0]), ndm2 = make_float2(-sc[1], -sc[1]);
                 const uint32_t dcol = P::D1COL + (s & 1) * BN + half * 64;
