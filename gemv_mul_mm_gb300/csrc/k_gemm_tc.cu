@@ -13,7 +13,9 @@
 //   * warps 2-5 (one thread per weight row) decode the raw bytes in registers
 //     into f16 INTEGER CODES -- the stored code times its integer sub-scale, or
 //     the codebook value -- and store them straight into tensor memory (the
-//     row's TMEM lane), plus the fp32 scales of the row into shared memory;
+//     row's TMEM lane), plus the fp32 scales of the row into shared memory; in
+//     the super-block kernel most formats add warps 16-19, a second decoder
+//     set that takes every other super-step;
 //   * warp 1 (one elected thread) issues tcgen05.mma kind::f16 with A = codes
 //     from TMEM and B = activations from shared memory into fp32 TMEM
 //     accumulators, one fresh accumulator per promotion unit;
