@@ -61,6 +61,45 @@ class Wait:
         return c == self.target + 1
 
 
+def simulate(model, actors, rng):
+    """Runs `actors` (generators that yield a Wait, or None to let others
+    run) against the model's asynchronous work: `model.loads` (callables,
+    landing in any order) and `model.fifo` (completed in order by
+    `model.complete()`). Each actor and each kind of completion gets its own
+    speed, so that one role can run far ahead of another."""
+    speed = [rng.uniform(0.02, 1.0) for _ in range(len(actors) + 2)]
+    blocked = [None] * len(actors)
+    live = list(range(len(actors)))
+    idle = 0
+    while live or model.loads or model.fifo:
+        cand = [("a", k) for k in live] + [("l", None)] * bool(model.loads) + [("m", None)] * bool(model.fifo)
+        w = [speed[k] if t == "a" else speed[-1 if t == "l" else -2] for t, k in cand]
+        t, k = rng.choices(cand, weights=w)[0]
+        if t == "l":
+            model.loads.pop(rng.randrange(len(model.loads)))()
+            idle = 0
+            continue
+        if t == "m":
+            model.complete()
+            idle = 0
+            continue
+        if blocked[k] is not None:
+            if not blocked[k].poll():
+                idle += 1
+                if idle > 200000:
+                    raise Violation("no progress: the protocol deadlocks")
+                continue
+            blocked[k] = None
+        idle = 0
+        try:
+            req = next(actors[k])
+        except StopIteration:
+            live.remove(k)
+            continue
+        if isinstance(req, Wait):
+            blocked[k] = req
+
+
 class Model:
     def __init__(self, nsup, NS, RS, sets, mins, per_stage_done=False, raw_prewait=True):
         self.nsup, self.NS, self.RS, self.sets, self.mins = nsup, NS, RS, sets, mins
@@ -86,7 +125,7 @@ class Model:
         self.D1 = [None, None]
         self.D2 = None
         self.handoff = None          # half-step handed from the waiter to the issuer
-        self.mma_fifo = []           # issued MMA groups, completing in order
+        self.fifo = []               # issued MMA groups, completing in order
         self.loads = []              # copies in flight, landing in any order
 
     # which completion barrier and phase signal "half-step h has completed"
@@ -168,7 +207,7 @@ class Model:
                 yield None
             self.handoff = None
             self.check_operands(h)
-            self.mma_fifo.append(h)
+            self.fifo.append(h)
 
     def check_operands(self, h):
         i, half, s = h % self.NS, h & 1, h >> 1
@@ -180,8 +219,8 @@ class Model:
             if any(m != s for m in self.amin) or self.bmin != s:
                 raise Violation(f"MMA {h}: min tiles hold {self.amin} / {self.bmin}")
 
-    def complete_mma(self):
-        h = self.mma_fifo.pop(0)
+    def complete(self):
+        h = self.fifo.pop(0)
         self.check_operands(h)                              # nothing overwritten in flight
         half, s = h & 1, h >> 1
         b = s & 1
@@ -210,44 +249,11 @@ class Model:
             self.d_empty[s & 1].arrive()
             self.sc_empty[s % SCD].arrive()
 
-    # ------------------------------------------------------------- scheduler
     def run(self, rng):
         actors = [self.producer_raw(), self.producer_x(), self.waiter(), self.issuer()]
         actors += [self.decoder(d, q) for d in range(self.sets) for q in range(NDEC_WARPS)]
         actors += [self.epilogue(e) for e in range(NEPI_WARPS)]
-        # every actor (and the two kinds of asynchronous completion) gets its
-        # own speed, so that one role can run far ahead of another
-        speed = [rng.uniform(0.02, 1.0) for _ in range(len(actors) + 2)]
-        blocked = [None] * len(actors)
-        live = list(range(len(actors)))
-        idle = 0
-        while live or self.loads or self.mma_fifo:
-            cand = [("a", k) for k in live] + [("l", None)] * bool(self.loads) + [("m", None)] * bool(self.mma_fifo)
-            w = [speed[k] if t == "a" else speed[-1 if t == "l" else -2] for t, k in cand]
-            t, k = rng.choices(cand, weights=w)[0]
-            if t == "l":
-                self.loads.pop(rng.randrange(len(self.loads)))()
-                idle = 0
-                continue
-            if t == "m":
-                self.complete_mma()
-                idle = 0
-                continue
-            if blocked[k] is not None:
-                if not blocked[k].poll():
-                    idle += 1
-                    if idle > 200000:
-                        raise Violation("no progress: the protocol deadlocks")
-                    continue
-                blocked[k] = None
-            idle = 0
-            try:
-                req = next(actors[k])
-            except StopIteration:
-                live.remove(k)
-                continue
-            if isinstance(req, Wait):
-                blocked[k] = req
+        simulate(self, actors, rng)
 
 
 # (stages, raw stages, decoder sets, min term): every combination the kernel
@@ -457,37 +463,7 @@ class Model32:
         actors = [self.producer_raw(), self.producer_x(), self.waiter(), self.issuer()]
         actors += [self.decoder(q) for q in range(NDEC_WARPS)]
         actors += [self.epilogue(e) for e in range(NEPI_WARPS)]
-        speed = [rng.uniform(0.02, 1.0) for _ in range(len(actors) + 2)]
-        blocked = [None] * len(actors)
-        live = list(range(len(actors)))
-        idle = 0
-        while live or self.loads or self.fifo:
-            cand = [("a", k) for k in live] + [("l", None)] * bool(self.loads) + [("m", None)] * bool(self.fifo)
-            w = [speed[k] if t == "a" else speed[-1 if t == "l" else -2] for t, k in cand]
-            t, k = rng.choices(cand, weights=w)[0]
-            if t == "l":
-                self.loads.pop(rng.randrange(len(self.loads)))()
-                idle = 0
-                continue
-            if t == "m":
-                self.complete()
-                idle = 0
-                continue
-            if blocked[k] is not None:
-                if not blocked[k].poll():
-                    idle += 1
-                    if idle > 200000:
-                        raise Violation("no progress: the protocol deadlocks")
-                    continue
-                blocked[k] = None
-            idle = 0
-            try:
-                req = next(actors[k])
-            except StopIteration:
-                live.remove(k)
-                continue
-            if isinstance(req, Wait):
-                blocked[k] = req
+        simulate(self, actors, rng)
 
 
 # (raw stages, activation stages, accumulators, min term): the stage counts the
