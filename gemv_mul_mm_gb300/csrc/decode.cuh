@@ -298,7 +298,7 @@ __device__ __forceinline__ float codebook_entry(int c) {
 //   Q4_0    q - 8                                    d        per 32
 //   Q5_0    q - 16                                   d        per 32
 //   IQ4_NL  KV[c]                                    d        per 32
-//   MXFP4   E2M1[c] * 2^(e - e_max)  (exact unless e_max - e > 24)   2^(e_max-127) per 256
+//   MXFP4   E2M1[c] * 2^(e - e_max)  (exact while e_max - e <= 23)  2^(e_max-127) per 256
 //   Q8_1    q                                        d        per 32
 //   Q4_1    q                                        d        per 32;   mins: m (an f16)
 //   Q5_1    q                                        d        per 32;   mins: m (an f16)

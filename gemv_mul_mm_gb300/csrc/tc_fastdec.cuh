@@ -316,7 +316,9 @@ template <> struct FastDec<IQ4_NL> {
 // 256-element super-step are folded into the operands relative to the largest
 // one, e_max (2^(e_max - 127) multiplies the super-block's partial sums): a
 // block's codes are scaled by 2^-(e_max - e), an exact f16 power of two (zero
-// below 2^-24, when the exponents of one super-step span more than 24).
+// below 2^-24, when the exponents of one super-step span more than 24). The
+// operand E2M1 * 2^-(e_max - e) is exact for spreads up to 23; at 24 the codes
+// +-0.5 and +-1.5 round to even.
 __device__ __forceinline__ uint32_t h2pow2neg(uint32_t k) {
     const uint32_t h = k <= 14u ? ((15u - k) << 10) : (k <= 24u ? (1u << (24u - k)) : 0u);
     return h | (h << 16);

@@ -203,3 +203,28 @@ def test_products_exact_at_extreme_codes(orc, kind):
     want = (exact - dmin.astype(np.float64) * mn.astype(np.float64)).astype(np.float32)
     deq = orc.dequant(kind, b.reshape(-1), 4, be)
     assert np.array_equal(deq.view(np.uint32), want.view(np.uint32))
+
+
+def test_mxfp4_operand_fold_range():
+    """The tensor-core GEMM folds each MXFP4 block's exponent into its f16
+    operands relative to the largest exponent e_max of the 256-element
+    super-step: operand = E2M1 value * 2^-(e_max - e), rounded once to f16.
+    An E2M1 value is m * 2^-1 with m <= 12, so the operand is exact while the
+    spread e_max - e is at most 23 (f16 subnormals are the multiples of
+    2^-24); at 24 the odd halves (+-0.5, +-1.5) round to even; past 24 the
+    kernel zeroes the scale and the block contributes nothing. The scale words
+    themselves are f16 powers of two down to 2^-24 (normal through 2^-14,
+    subnormal below)."""
+    for d in range(0, 24):
+        exact = KV_E2M1.astype(np.float64) * 2.0 ** -d
+        assert np.array_equal(exact.astype(np.float16).astype(np.float64), exact), d
+    at24 = KV_E2M1.astype(np.float64) * 2.0 ** -24
+    r = at24.astype(np.float16).astype(np.float64)
+    odd_half = np.isin(np.abs(KV_E2M1), [0.5, 1.5])
+    assert np.array_equal(r[~odd_half], at24[~odd_half])
+    assert np.array_equal(np.abs(r[odd_half]), np.where(np.abs(KV_E2M1[odd_half]) == 0.5, 0.0, 2.0 ** -23))
+    # the scale word for a spread k: f16 bits (15 - k) << 10 (normal) or
+    # 1 << (24 - k) (subnormal), 2^-k either way
+    for k in range(0, 25):
+        bits = ((15 - k) << 10) if k <= 14 else (1 << (24 - k))
+        assert np.array([bits], np.uint16).view(np.float16)[0] == np.float16(2.0 ** -k), k

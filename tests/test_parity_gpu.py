@@ -682,9 +682,10 @@ def test_operand_fold_worst_case(Q, orc, kind):
 @pytest.mark.parametrize("lo,hi", [(100, 140), (103, 127), (118, 142)])
 def test_mxfp4_exponent_spread_on_tensor_cores(Q, orc, lo, hi):
     """MXFP4 on the tensor cores folds each block's exponent into its operands
-    relative to the largest of its 256-element super-step: spreads beyond 24
-    flush the smallest blocks' operands (f16 subnormals end at 2^-24), which
-    stays far inside the bar; spreads up to 24 are exact."""
+    relative to the largest of its 256-element super-step: spreads up to 23
+    are exact; at 24 the odd halves round, beyond it a block contributes
+    nothing (f16 subnormals end at 2^-24). With random codes the largest
+    block dominates and the loss stays far inside the bar."""
     M, K, N = 256, 4096, 40
     w = synth.quant_weights("MXFP4", M, K, 31 + lo, e8m0_lo=lo, e8m0_hi=hi)
     x = synth.activations(N, K, 32 + lo, "f16")
