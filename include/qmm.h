@@ -171,6 +171,14 @@ QMM_API int qgemv(int kind, const void* W, size_t w_bytes, const void* x, int x_
  *   Y            device fp32, N * M elements; y_elems its size
  *
  * Accuracy: |Y - Y_exact| <= 1e-3 * sum_k |W[m,k] * X[n,k]| + 1e-6 per element.
+ * One condition on the tensor-core path: MXFP4 folds each block's exponent
+ * into its f16 operands relative to the largest exponent of its 256-element
+ * group. This is exact while the eight exponents of a group span at most 23.
+ * At 24 the codes +-0.5 and +-1.5 of the smallest block round to even; a block
+ * 25 or more below the largest contributes nothing. The bound then holds while
+ * the group's largest-exponent block carries a nonzero code against
+ * activations of comparable magnitude (quantizers derive a block's exponent
+ * from its largest value). The GEMV (N <= 8) and qdequant have no such limit.
  *
  * Workspace: the tensor-core path keeps its scratch in a per-device workspace
  * the library owns and grows on demand (cudaMalloc): the f16 (hi, lo) rows of
